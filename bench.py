@@ -1,0 +1,474 @@
+#!/usr/bin/env python3
+"""Benchmark of the attention hot path on GB300.
+
+One step = one forward + one backward (atomic-dQ mode) of exact causal
+attention on the bf16 training shape b=4, s=8192, hq=32, hkv=8, d=128
+(GQA 4:1), inputs resident in HBM.  The headline value is TFLOP/s counted
+with the FlashAttention FAQ's causal formula (Inference Cookbook Q16):
+4*b*hq*s*s*d/2 for the forward and 2.5x that for the backward.
+
+Also measured on the same run (each in its own timed loop): forward alone,
+backward alone, the deterministic backward, the varlen workload, the paged
+decode workload (HBM GB/s), an end-to-end pass through the public API from
+pinned host buffers, and the float64 CPU oracle on a bounded sample.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+Under torchrun each rank runs its own replica (weak scaling) and rank 0
+prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/fwd+bwd TFLOP/s, bf16 causal N=8k d=128; % of GB300 tensor peak"
+B, S, HQ, HKV, D = 4, 8192, 32, 8, 128
+FWD_FLOPS = 4 * B * HQ * S * S * D / 2          # 2.199e12
+BWD_FLOPS = 2.5 * FWD_FLOPS                     # 5.498e12
+STEP_FLOPS = FWD_FLOPS + BWD_FLOPS
+WORKLOAD = "training fwd+bwd, bf16, causal, b=4 s=8192 hq=32 hkv=8 d=128 (GQA 4:1), atomic dQ"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while a timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ helpers
+
+
+def sources_sha(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "exact_attention_41_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_key):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's
+    sources are unchanged since that capture; else None."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "dram_traffic.json")) as f:
+            t = json.load(f)[kernel_key]
+        if sources_sha(t["sources"]) != t["sources_sha256"]:
+            return None
+        return t["bytes_per_launch"]
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def timed(fn, steps, stream):
+    import torch
+
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        fn()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def dev_normal(shape, seed, dtype):
+    import torch
+
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    return torch.randn(shape, generator=g, device="cuda", dtype=torch.float32).to(dtype)
+
+
+# ------------------------------------------------------------------ workloads
+
+
+def training_inputs():
+    import torch
+
+    bf = torch.bfloat16
+    q = dev_normal((B, S, HQ, D), 60, bf)
+    k = dev_normal((B, S, HKV, D), 61, bf)
+    v = dev_normal((B, S, HKV, D), 62, bf)
+    do = dev_normal((B, S, HQ, D), 63, bf)
+    return q, k, v, do
+
+
+def bench_varlen(libattn, steps, stream):
+    import numpy as np
+    import torch
+
+    from exact_attention_41_gb300 import synthetic as syn
+
+    lens = syn.varlen_lengths(7)
+    cu = torch.from_numpy(syn.cu_seqlens(lens)).cuda()
+    t = int(lens.sum())
+    bf = torch.bfloat16
+    q, k, v, do = (dev_normal((t, h, D), 70 + i, bf) for i, h in enumerate((HQ, HKV, HKV, HQ)))
+    kw = dict(causal=True, window=(256, 0), softcap=50.0)
+    mx = int(lens.max())
+    o, lse = libattn.fwd_varlen(q, k, v, cu, cu, mx, mx, **kw)
+    ws = torch.empty(libattn.lib().attn_bwd_varlen_workspace_size(len(lens), mx, mx, t, t, HQ,
+                                                                  HKV, D, 0),
+                     device="cuda", dtype=torch.uint8)
+    # visible (query, key) pairs per head: sum over sequences of min(i + 1, 257)
+    pairs = sum(int(np.minimum(np.arange(n) + 1, 257).sum()) for n in lens)
+    flops_f = 4.0 * HQ * D * pairs
+
+    def f():
+        libattn.fwd_varlen(q, k, v, cu, cu, mx, mx, out=o, lse=lse, **kw)
+
+    def fb():
+        f()
+        libattn.bwd_varlen(q, k, v, o, lse, do, cu, cu, mx, mx, workspace=ws, **kw)
+
+    for _ in range(2):
+        fb()
+    tf = timed(f, steps, stream)
+    tfb = timed(fb, steps, stream)
+    return {"workload": "varlen 64 seqs U[100,4096] (seed 7), bf16, hq=32 hkv=8 d=128, causal, "
+                        "window (256,0), softcap 50",
+            "tokens": t, "visible_pairs_per_head": pairs,
+            "fwd_ms": round(tf, 4), "fwd_tflops": round(flops_f / tf / 1e9, 2),
+            "fwd_bwd_ms": round(tfb, 4), "fwd_bwd_tflops": round(3.5 * flops_f / tfb / 1e9, 2),
+            "flops_note": "algorithmic: 4*hq*d*visible pairs (fwd), x2.5 bwd"}
+
+
+def bench_decode(libattn, steps, stream, sq):
+    import numpy as np
+    import torch
+
+    from exact_attention_41_gb300 import synthetic as syn
+
+    b, page = 64, 256
+    seqlens, table, npages = syn.decode_layout(8, b, 32768, page, sq)
+    bf = torch.bfloat16
+    kc = dev_normal((npages, page, HKV, D), 80, bf)
+    vc = dev_normal((npages, page, HKV, D), 81, bf)
+    q = dev_normal((b, sq, HQ, D), 82, bf)
+    kn = dev_normal((b, sq, HKV, D), 83, bf)
+    vn = dev_normal((b, sq, HKV, D), 84, bf)
+    sl = torch.from_numpy(seqlens).cuda()
+    bt = torch.from_numpy(table).cuda()
+    splits = libattn.num_splits(b, sq, HQ, HKV, D, table.shape[1] * page, 0)
+    ws = libattn.kvcache_workspace(q, kc, page, table.shape[1], 0)
+    o = torch.empty_like(q)
+    lse = torch.empty((b, HQ, sq), device="cuda", dtype=torch.float32)
+
+    def f():
+        libattn.fwd_kvcache(q, kc, vc, sl, k_new=kn, v_new=vn, block_table=bt, causal=True,
+                            workspace=ws, out=o, lse=lse)
+
+    for _ in range(3):
+        f()
+    # flush L2 between reps is unnecessary: 8.6 GB of K/V per step >> L2
+    t = timed(f, steps, stream)
+    kv_bytes = int((seqlens.astype(np.int64) + sq).sum()) * HKV * D * 2 * 2
+    io_bytes = (2 * b * sq * HQ * D * 2 + b * HQ * sq * 4      # q read, out write, lse
+                + 2 * b * sq * HKV * D * 2)                    # k_new/v_new read (cache write
+    #                                                            counted in kv_bytes read side)
+    total = kv_bytes + io_bytes
+    return {"workload": f"paged decode bf16 b=64 sq=s_new={sq} hq=32 hkv=8 d=128, "
+                        "cache_seqlens U[1,32768] (seed 8), 256-token pages, causal",
+            "num_splits": splits, "ms": round(t, 4), "bytes": total,
+            "gbs": round(total / t / 1e6, 1), "tokens_per_s": round(b * sq / t * 1e3, 1)}
+
+
+def cpu_baseline_sample(repeat=1):
+    """The float64 oracle on a bounded sample of the training workload: the
+    forward and backward of one (batch, head) at s=8192, causal."""
+    import numpy as np
+
+    from exact_attention_41_gb300 import synthetic as syn
+    from oracle import attention as ref
+
+    rng = np.random.default_rng(90)
+    q, k, v, do = (syn.bits_to_f64(syn.normal_bits(rng, (S, D), syn.BF16), syn.BF16)
+                   for _ in range(4))
+    t0 = time.perf_counter()
+    for _ in range(repeat):
+        ref.head_forward(q, k, v, np.arange(S), S, S, 1 / math.sqrt(D), causal=True)
+        ref.head_backward(q, k, v, do, S, S, 1 / math.sqrt(D), causal=True)
+    dt = (time.perf_counter() - t0) / repeat
+    flops = STEP_FLOPS / (B * HQ)
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "kind": "oracle",
+            "sample": "float64 oracle fwd+bwd of one (batch, head) of the training shape "
+                      f"(s=8192, d=128, causal), {dt:.2f} s; algorithmic causal FLOPs "
+                      f"{flops:.3e}; numpy/BLAS on all host threads"}
+
+
+# ------------------------------------------------------------------ arms
+
+
+def run_reference(args, rank):
+    """The float64 oracle as it stands, on the host cores: each step is a
+    bounded sample of the training workload, the causal attention (forward
+    and backward) of the first 4096 tokens of one (batch, head)."""
+    if rank != 0:
+        return
+    import numpy as np
+
+    from exact_attention_41_gb300 import synthetic as syn
+    from oracle import attention as ref
+
+    n = 4096
+    rng = np.random.default_rng(90)
+    q, k, v, do = (syn.bits_to_f64(syn.normal_bits(rng, (n, D), syn.BF16), syn.BF16)
+                   for _ in range(4))
+
+    def step():
+        ref.head_forward(q, k, v, np.arange(n), n, n, 1 / math.sqrt(D), causal=True)
+        ref.head_backward(q, k, v, do, n, n, 1 / math.sqrt(D), causal=True)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    flops = 3.5 * 4 * n * n * D / 2
+    value = flops / dt / 1e12
+    sample = (f"float64 oracle fwd+bwd per step of the causal prefix of {n} tokens of one "
+              "(batch, head) of the training shape (d=128); algorithmic causal FLOPs "
+              f"{flops:.3e}; numpy/BLAS on all host threads")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "parallelism": "host cores",
+                   "sample": f"causal prefix of {n} tokens of one (batch, head) per step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    from exact_attention_41_gb300 import build as build_mod
+
+    if rank == 0 or world == 1:
+        build_mod.build()
+    if world > 1:
+        dist.barrier()
+    from exact_attention_41_gb300 import libattn
+
+    pk = peaks()
+    stream = torch.cuda.current_stream()
+    q, k, v, do = training_inputs()
+    o = torch.empty_like(q)
+    lse = torch.empty((B, HQ, S), device="cuda", dtype=torch.float32)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = libattn.bwd_workspace(q, k, False)
+    ws_det = libattn.bwd_workspace(q, k, True)
+
+    def fwd():
+        libattn.fwd(q, k, v, causal=True, out=o, lse=lse)
+
+    def bwd(det=False):
+        libattn.bwd(q, k, v, o, lse, do, causal=True, deterministic=det,
+                    workspace=ws_det if det else ws, dq=dq, dk=dk, dv=dv)
+
+    def step():
+        fwd()
+        bwd()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    n0 = libattn.launch_count()
+    with ClockSampler(local_rank) as clk:
+        ms = timed(step, args.steps, stream)
+    launches = libattn.launch_count() - n0
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * STEP_FLOPS / (ms * 1e-3) / 1e12
+
+    extra_steps = max(5, min(args.steps, 20))
+    ms_fwd = timed(fwd, extra_steps, stream)
+    ms_bwd = timed(bwd, extra_steps, stream)
+    ms_bwd_det = timed(lambda: bwd(True), extra_steps, stream)
+
+    # end to end through the public API from pinned host buffers
+    hq_, hk_, hv_, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
+    rq, rk, rv = (torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (dq, dk, dv))
+    h2d = sum(x.numel() * x.element_size() for x in (hq_, hk_, hv_, hdo))
+    d2h = sum(x.numel() * x.element_size() for x in (rq, rk, rv))
+
+    def e2e_step():
+        q.copy_(hq_, non_blocking=True)
+        k.copy_(hk_, non_blocking=True)
+        v.copy_(hv_, non_blocking=True)
+        do.copy_(hdo, non_blocking=True)
+        step()
+        rq.copy_(dq, non_blocking=True)
+        rk.copy_(dk, non_blocking=True)
+        rv.copy_(dv, non_blocking=True)
+
+    e2e_step()
+    ms_e2e = timed(e2e_step, extra_steps, stream)
+
+    out = None
+    if rank == 0:
+        peak_t = pk["bf16_tflops"]
+        bwd_tflops = BWD_FLOPS / (ms_bwd * 1e-3) / 1e12
+        fwd_tflops = FWD_FLOPS / (ms_fwd * 1e-3) / 1e12
+        out = {
+            "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: N(0,1) bf16 from torch's seeded CUDA generator",
+            "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": S,
+                       "heads_q": HQ, "heads_kv": HKV, "head_dim": D,
+                       "parallelism": f"replicas x{world} (no collective on the data path)",
+                       "l2": "no flush: each step reads >= 896 MiB of inputs, above the 126 MB L2"},
+            "frac_of_peak": round(value / world / pk["bf16_tflops_sustained"], 4),
+            "peak_note": f"bf16 dense, {pk['source']} (sustained for the step, burst per kernel)",
+            "tokens_per_s": round(world * B * S / (ms * 1e-3), 1),
+            "fwd": {"ms": round(ms_fwd, 4), "tflops": round(fwd_tflops, 2),
+                    "frac": round(fwd_tflops / peak_t, 4)},
+            "bwd": {"ms": round(ms_bwd, 4), "tflops": round(bwd_tflops, 2),
+                    "frac": round(bwd_tflops / peak_t, 4)},
+            "bwd_deterministic": {"ms": round(ms_bwd_det, 4),
+                                  "tflops": round(BWD_FLOPS / (ms_bwd_det * 1e-3) / 1e12, 2)},
+            "roofline": {"bound": "tensor", "kernel": "backward (attn_bwd call)",
+                         "achieved": round(bwd_tflops, 2), "peak": peak_t, "unit": "TFLOP/s",
+                         "frac": round(bwd_tflops / peak_t, 4),
+                         "traffic": traffic_for("bwd"),
+                         "per_launch": "algorithmic bwd FLOPs 5.498e12 / CUDA-event time of "
+                                       "one attn_bwd call"},
+            "roofline_fwd": {"bound": "tensor", "kernel": "forward (attn_fwd call)",
+                             "achieved": round(fwd_tflops, 2), "peak": peak_t, "unit": "TFLOP/s",
+                             "frac": round(fwd_tflops / peak_t, 4), "traffic": traffic_for("fwd")},
+            "e2e": {"value": round(world * STEP_FLOPS / (ms_e2e * 1e-3) / 1e12, 2),
+                    "unit": "TFLOP/s", "ms_per_step": round(ms_e2e, 4),
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches,
+            "clocks": clk.summary(),
+        }
+    del hq_, hk_, hv_, hdo, rq, rk, rv, ws_det
+    if rank == 0 and not args.no_extras:
+        del q, k, v, do, o, lse, dq, dk, dv, ws
+        torch.cuda.empty_cache()
+        out["varlen"] = bench_varlen(libattn, extra_steps, stream)
+        torch.cuda.empty_cache()
+        for sq in (1, 4):
+            r = bench_decode(libattn, extra_steps, stream, sq)
+            r["frac_of_hbm"] = round(r["gbs"] / pk["hbm_gbs"], 4)
+            out[f"decode_sq{sq}"] = r
+            torch.cuda.empty_cache()
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_sample()
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-extras", action="store_true", help="skip varlen/decode lines")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,53 @@
+// Internal launcher interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include "common.cuh"
+
+namespace attn {
+
+// One dense or packed (varlen) attention problem.
+struct FwdArgs {
+  const void *q, *k, *v;
+  void *o;
+  float *lse;
+  Seqs seqs;
+  int batch, hq, hkv, d, dtype;
+  float scale, softcap;  // softcap <= 0: off
+  int win_l, win_r;      // -1 = unbounded; causal already folded into win_r = 0
+  int *err;              // device error word
+};
+
+struct BwdArgs {
+  FwdArgs f;             // f.o / f.lse are the forward's outputs (read only)
+  const void *dout;
+  void *dq, *dk, *dv;
+  float *dsum;           // workspace: D_i = rowsum(dO * O), LSE layout
+  float *dq_acc;         // workspace: fp32 dQ accumulator (atomic mode)
+  int deterministic;
+};
+
+struct DecodeArgs {
+  const void *q;
+  void *k_cache, *v_cache;
+  const void *k_new, *v_new;
+  const int32_t *cache_seqlens, *block_table;
+  int num_pages, page_size, max_pages;
+  void *o;
+  float *lse;
+  int dtype, b, sq, s_new, hq, hkv, d;
+  float scale, softcap;
+  int win_l, win_r;
+  int num_splits, split_chunk;  // keys per split (multiple of 128)
+  float *o_part;                // (splits, b, sq, hq, d) fp32 when num_splits > 1
+  float *lse_part;              // (splits, b, hq, sq)
+  int *err;
+};
+
+// Adds n to the library's launch counter (attn_launch_count).
+void count_launches(int n);
+
+cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t st);
+cudaError_t launch_bwd_simt(const BwdArgs &a, cudaStream_t st);
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
+
+}  // namespace attn

@@ -1,0 +1,269 @@
+"""Thin ctypes binding over libattn.so (argument marshalling only).
+
+Every step of the computation runs in the CUDA library; this module checks
+tensor shapes, allocates outputs and workspaces with PyTorch (device memory
+and streams are all PyTorch is used for) and passes raw device pointers and
+the current CUDA stream to the C entry points of ``include/libattn.h``.
+
+There is no fallback: if the library is missing or a call fails, an
+exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import re
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "libattn.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "libattn.h")
+
+F16, BF16 = 0, 1
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported configuration",
+          3: "workspace missing or too small", 4: "CUDA error", 5: "device wait timed out",
+          6: "device-side data check failed"}
+
+_vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_SIGS = {
+    "attn_version": ([], ctypes.c_char_p),
+    "attn_status_str": ([_i], ctypes.c_char_p),
+    "attn_fwd": ([_vp] * 5 + [_i] * 7 + [_f, _i, _i, _i, _f, _vp], _i),
+    "attn_bwd_workspace_size": ([_i] * 7, _sz),
+    "attn_bwd": ([_vp] * 9 + [_i] * 7 + [_f, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
+    "attn_fwd_varlen": ([_vp] * 7 + [_i] * 9 + [_f, _i, _i, _i, _f, _vp], _i),
+    "attn_bwd_varlen_workspace_size": ([_i] * 9, _sz),
+    "attn_bwd_varlen": ([_vp] * 11 + [_i] * 9 + [_f, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
+    "attn_kvcache_num_splits": ([_i] * 7, _i),
+    "attn_kvcache_workspace_size": ([_i] * 7, _sz),
+    "attn_fwd_kvcache": ([_vp] * 7 + [_i] * 3 + [_vp, _vp] + [_i] * 7 +
+                         [_f, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
+    "attn_get_device_error": ([_vp, ctypes.POINTER(_i)], _i),
+    "attn_launch_count": ([], ctypes.c_ulonglong),
+}
+
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)} (status {status})")
+        self.status = status
+
+
+def header_functions() -> list[str]:
+    """Names of the functions include/libattn.h declares."""
+    with open(HEADER) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^(?:[a-z_0-9]+\s+)+\*?\s*(attn_[a-z0-9_]+)\s*\(",
+                                 text, flags=re.M)))
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libattn.so (built by ``__graft_entry__.build()``); raises if absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"libattn.so is not built ({LIB_PATH}); run __graft_entry__.build()")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (args, res) in _SIGS.items():
+            fn = getattr(l, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = l
+    return _lib
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise AttnError(status, what)
+
+
+def _torch():
+    import torch
+
+    return torch
+
+
+def _dt(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.float16:
+        return F16
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"dtype {t.dtype} is not fp16/bf16")
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(_torch().cuda.current_stream().cuda_stream)
+
+
+def _need(cond, msg):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _cuda_contig(*ts):
+    for t in ts:
+        if t is not None:
+            _need(t.is_cuda, "tensors must be on a CUDA device")
+            _need(t.is_contiguous(), "tensors must be contiguous (Inference Cookbook FAQ Q13)")
+
+
+def _win(window):
+    wl, wr = window
+    return int(wl), int(wr)
+
+
+def _scale(scale, d):
+    return 1.0 / math.sqrt(d) if scale is None else float(scale)
+
+
+def fwd(q, k, v, *, scale=None, causal=False, window=(-1, -1), softcap=0.0, out=None, lse=None):
+    """Dense forward.  q (b,sq,hq,d), k/v (b,sk,hkv,d) -> out (b,sq,hq,d), lse (b,hq,sq) fp32."""
+    torch = _torch()
+    b, sq, hq, d = q.shape
+    _, sk, hkv, _ = k.shape
+    _need(k.shape == v.shape and k.shape[0] == b and k.shape[3] == d, "k/v shape mismatch")
+    _need(q.dtype == k.dtype == v.dtype, "q, k, v must share a dtype")
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((b, hq, sq), device=q.device, dtype=torch.float32) if lse is None else lse
+    _cuda_contig(q, k, v, out, lse)
+    wl, wr = _win(window)
+    st = lib().attn_fwd(_p(q), _p(k), _p(v), _p(out), _p(lse), _dt(q), b, sq, sk, hq, hkv, d,
+                        _scale(scale, d), int(bool(causal)), wl, wr, float(softcap), _stream())
+    _check(st, "attn_fwd")
+    return out, lse
+
+
+def bwd_workspace(q, k, deterministic=False):
+    torch = _torch()
+    b, sq, hq, d = q.shape
+    n = lib().attn_bwd_workspace_size(b, sq, k.shape[1], hq, k.shape[2], d, int(bool(deterministic)))
+    return torch.empty(max(n, 1), device=q.device, dtype=torch.uint8)
+
+
+def bwd(q, k, v, out, lse, dout, *, scale=None, causal=False, window=(-1, -1), softcap=0.0,
+        deterministic=False, workspace=None, dq=None, dk=None, dv=None):
+    """Dense backward -> dq, dk, dv (same shapes and dtype as q, k, v)."""
+    torch = _torch()
+    b, sq, hq, d = q.shape
+    _, sk, hkv, _ = k.shape
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws = bwd_workspace(q, k, deterministic) if workspace is None else workspace
+    _cuda_contig(q, k, v, out, lse, dout, dq, dk, dv, ws)
+    wl, wr = _win(window)
+    st = lib().attn_bwd(_p(q), _p(k), _p(v), _p(out), _p(lse), _p(dout), _p(dq), _p(dk), _p(dv),
+                        _dt(q), b, sq, sk, hq, hkv, d, _scale(scale, d), int(bool(causal)), wl,
+                        wr, float(softcap), int(bool(deterministic)), _p(ws), ws.numel(),
+                        _stream())
+    _check(st, "attn_bwd")
+    return dq, dk, dv
+
+
+def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, *, scale=None,
+               causal=False, window=(-1, -1), softcap=0.0, out=None, lse=None):
+    """Packed forward.  q (Tq,hq,d), k/v (Tk,hkv,d) -> out (Tq,hq,d), lse (hq,Tq)."""
+    torch = _torch()
+    tq, hq, d = q.shape
+    tk, hkv, _ = k.shape
+    batch = cu_seqlens_q.numel() - 1
+    _need(cu_seqlens_q.dtype == torch.int32 and cu_seqlens_k.dtype == torch.int32,
+          "cu_seqlens must be int32")
+    _need(cu_seqlens_k.numel() == batch + 1, "cu_seqlens_q/k length mismatch")
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((hq, tq), device=q.device, dtype=torch.float32) if lse is None else lse
+    _cuda_contig(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_k)
+    wl, wr = _win(window)
+    st = lib().attn_fwd_varlen(_p(q), _p(k), _p(v), _p(out), _p(lse), _p(cu_seqlens_q),
+                               _p(cu_seqlens_k), batch, int(max_seqlen_q), int(max_seqlen_k), tq,
+                               tk, _dt(q), hq, hkv, d, _scale(scale, d), int(bool(causal)), wl,
+                               wr, float(softcap), _stream())
+    _check(st, "attn_fwd_varlen")
+    return out, lse
+
+
+def bwd_varlen(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k,
+               *, scale=None, causal=False, window=(-1, -1), softcap=0.0, deterministic=False,
+               workspace=None):
+    torch = _torch()
+    tq, hq, d = q.shape
+    tk, hkv, _ = k.shape
+    batch = cu_seqlens_q.numel() - 1
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    if workspace is None:
+        n = lib().attn_bwd_varlen_workspace_size(batch, int(max_seqlen_q), int(max_seqlen_k), tq,
+                                                 tk, hq, hkv, d, int(bool(deterministic)))
+        workspace = torch.empty(max(n, 1), device=q.device, dtype=torch.uint8)
+    _cuda_contig(q, k, v, out, lse, dout, cu_seqlens_q, cu_seqlens_k, workspace)
+    wl, wr = _win(window)
+    st = lib().attn_bwd_varlen(_p(q), _p(k), _p(v), _p(out), _p(lse), _p(dout), _p(dq), _p(dk),
+                               _p(dv), _p(cu_seqlens_q), _p(cu_seqlens_k), batch,
+                               int(max_seqlen_q), int(max_seqlen_k), tq, tk, _dt(q), hq, hkv, d,
+                               _scale(scale, d), int(bool(causal)), wl, wr, float(softcap),
+                               int(bool(deterministic)), _p(workspace), workspace.numel(),
+                               _stream())
+    _check(st, "attn_bwd_varlen")
+    return dq, dk, dv
+
+
+def kvcache_workspace(q, k_cache, page_size, max_pages_per_seq, num_splits=0):
+    torch = _torch()
+    b, sq, hq, d = q.shape
+    hkv = k_cache.shape[2]
+    n = lib().attn_kvcache_workspace_size(b, sq, hq, hkv, d, page_size * max_pages_per_seq,
+                                          int(num_splits))
+    return torch.empty(max(n, 1), device=q.device, dtype=torch.uint8)
+
+
+def fwd_kvcache(q, k_cache, v_cache, cache_seqlens, *, k_new=None, v_new=None, block_table=None,
+                scale=None, causal=False, window=(-1, -1), softcap=0.0, num_splits=0,
+                workspace=None, out=None, lse=None):
+    """Decode against a (paged) KV cache, appending k_new/v_new (Inference
+    Cookbook FAQ Q17/Q18).  Does not modify cache_seqlens."""
+    torch = _torch()
+    b, sq, hq, d = q.shape
+    if block_table is not None:
+        num_pages, page_size, hkv, _ = k_cache.shape
+        max_pages = block_table.shape[1]
+        _need(block_table.dtype == torch.int32, "block_table must be int32")
+    else:
+        num_pages, page_size, hkv, _ = k_cache.shape
+        max_pages = 1
+    s_new = 0 if k_new is None else k_new.shape[1]
+    _need(cache_seqlens.dtype == torch.int32, "cache_seqlens must be int32")
+    out = torch.empty_like(q) if out is None else out
+    lse = torch.empty((b, hq, sq), device=q.device, dtype=torch.float32) if lse is None else lse
+    ws = kvcache_workspace(q, k_cache, page_size, max_pages, num_splits) if workspace is None \
+        else workspace
+    _cuda_contig(q, k_cache, v_cache, k_new, v_new, cache_seqlens, block_table, out, lse, ws)
+    wl, wr = _win(window)
+    st = lib().attn_fwd_kvcache(_p(q), _p(k_cache), _p(v_cache), _p(k_new), _p(v_new),
+                                _p(cache_seqlens), _p(block_table), num_pages, page_size,
+                                max_pages, _p(out), _p(lse), _dt(q), b, sq, s_new, hq, hkv, d,
+                                _scale(scale, d), int(bool(causal)), wl, wr, float(softcap),
+                                int(num_splits), _p(ws), ws.numel(), _stream())
+    _check(st, "attn_fwd_kvcache")
+    return out, lse
+
+
+def num_splits(b, sq, hq, hkv, d, max_seqlen_k, requested=0) -> int:
+    return lib().attn_kvcache_num_splits(b, sq, hq, hkv, d, max_seqlen_k, requested)
+
+
+def launch_count() -> int:
+    """Kernels the library has enqueued since it was loaded."""
+    return int(lib().attn_launch_count())
+
+
+def device_error() -> tuple[int, int]:
+    """(status, raw error word) of the sticky device error word; clears it."""
+    detail = ctypes.c_int(0)
+    st = lib().attn_get_device_error(_stream(), ctypes.byref(detail))
+    return st, detail.value

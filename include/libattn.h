@@ -1,0 +1,196 @@
+/*
+ * libattn -- exact scaled dot-product attention for NVIDIA GB300 (sm_103a).
+ *
+ * What is computed (every entry point below), for batch b, query head h and
+ * KV head kv = h / (hq / hkv)  (GQA: contiguous groups of query heads share
+ * one KV head):
+ *
+ *   s_ij = scale * <q_i, k_j>                       "FlashAttention完整说明" §一
+ *   s_ij = softcap * tanh(s_ij / softcap)  if softcap > 0, applied BEFORE the
+ *          mask (Inference Cookbook FAQ Q22)
+ *   mask: query i sits at key position p_i = i + (sk - sq)  (bottom-right
+ *          alignment, Inference Cookbook FAQ Q6) and sees key j iff
+ *          p_i - win_l <= j <= p_i + win_r   (FAQ Q21; -1 = unbounded side;
+ *          causal != 0 forces win_r = 0)
+ *   P = softmax over the visible keys, O = P V,  LSE_i = m_i + ln(l_i)
+ *          (the saved softmax statistics of "FlashAttention完整说明" §二.2)
+ *
+ * Rows with no visible key produce O = 0 and LSE = -inf and get zero
+ * gradient.  The score matrix is never written to memory: the kernels tile
+ * Q/K/V through shared memory and use an online softmax (§二.1), and the
+ * backward recomputes S and P from Q, K and the saved LSE (§二.2).
+ *
+ * Layout (Inference Cookbook FAQ Q5): q/out/dout/dq are (batch, seqlen_q,
+ * hq, d), k/v/dk/dv are (batch, seqlen_k, hkv, d), all contiguous, element
+ * type fp16 or bf16 (dtype below; "FlashAttention完整说明" §八: FP16/BF16
+ * only).  d must be 64, 128 or 256.  LSE is fp32 (batch, hq, seqlen_q); for
+ * the varlen calls it is (hq, total_q).  Accumulation is fp32; outputs are
+ * rounded to the element type with round-to-nearest-even.
+ *
+ * Ownership and streams: every pointer is a DEVICE pointer owned by the
+ * caller, except where noted.  The library allocates nothing and never
+ * synchronises the stream on these calls; scratch memory is a caller-owned
+ * `workspace` sized by the matching *_workspace_size query.  All work is
+ * enqueued on `stream` (NULL = the legacy default stream), so a call can be
+ * captured into a CUDA graph when its pointers stay fixed (Inference Cookbook
+ * FAQ Q19).
+ *
+ * Errors: arguments are validated on the host before anything is enqueued;
+ * an invalid call returns a nonzero status and launches nothing.  A launch
+ * failure returns ATTN_ERR_CUDA.  Data-dependent faults detected on the
+ * device (a block_table entry outside the page pool, a varlen length above the
+ * stated maximum, a bounded wait that timed out) skip the offending work and
+ * raise a sticky device error word, read and cleared by
+ * attn_get_device_error().
+ */
+#ifndef LIBATTN_H
+#define LIBATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *attn_stream_t;
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID = 1,     /* bad pointer, size or flag combination          */
+  ATTN_ERR_UNSUPPORTED = 2, /* valid request this build does not implement    */
+  ATTN_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required     */
+  ATTN_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed  */
+  ATTN_ERR_TIMEOUT = 5,     /* a device-side bounded wait expired             */
+  ATTN_ERR_DEVICE = 6       /* device-side data check failed (see above)      */
+} attn_status;
+
+enum { ATTN_F16 = 0, ATTN_BF16 = 1 };
+
+/* Library version string, e.g. "libattn 0.1.0 (sm_103a)".  Host only. */
+const char *attn_version(void);
+
+/* Human-readable name of a status code.  Host only. */
+const char *attn_status_str(attn_status s);
+
+/*
+ * Dense forward.  q (b,sq,hq,d), k/v (b,sk,hkv,d), out (b,sq,hq,d) in dtype;
+ * lse (b,hq,sq) fp32, required (the backward reads it).  sq == 0 or sk == 0
+ * is valid (sk == 0: every row is empty).  hq % hkv must be 0.
+ */
+attn_status attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+                     int dtype, int b, int sq, int sk, int hq, int hkv, int d, float scale,
+                     int causal, int win_l, int win_r, float softcap, attn_stream_t stream);
+
+/*
+ * Backward ("FlashAttention完整说明" §二.2: recompute S and P from Q, K and
+ * the saved LSE).  Inputs q, k, v, out, lse as produced by attn_fwd with the
+ * same arguments, dout (b,sq,hq,d).  Outputs dq (b,sq,hq,d), dk/dv
+ * (b,sk,hkv,d) in dtype, fully overwritten.
+ *
+ * deterministic != 0 makes dq bitwise reproducible run to run (no
+ * floating-point atomics, Inference Cookbook FAQ Q11); deterministic == 0
+ * may accumulate dq with fp32 atomics in an unspecified order.
+ *
+ * workspace: device scratch of at least attn_bwd_workspace_size(...) bytes,
+ * 256-byte aligned; its contents need not be initialised.
+ */
+size_t attn_bwd_workspace_size(int b, int sq, int sk, int hq, int hkv, int d, int deterministic);
+
+attn_status attn_bwd(const void *q, const void *k, const void *v, const void *out,
+                     const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                     int dtype, int b, int sq, int sk, int hq, int hkv, int d, float scale,
+                     int causal, int win_l, int win_r, float softcap, int deterministic,
+                     void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * Varlen (packed) forward, Inference Cookbook FAQ Q8.  q (total_q,hq,d),
+ * k/v (total_k,hkv,d), out (total_q,hq,d); lse (hq,total_q) fp32.
+ * cu_seqlens_q/k: DEVICE int32 arrays of batch+1 offsets starting at 0.
+ * Sequence i has sq_i = cu_q[i+1]-cu_q[i] queries and sk_i keys; its masks
+ * align bottom-right within the sequence.  max_seqlen_q/k must bound every
+ * sq_i/sk_i (a sequence that exceeds them is skipped and raises the device
+ * error word); total_q/total_k must equal cu_q[batch]/cu_k[batch].
+ */
+attn_status attn_fwd_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
+                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                            int batch, int max_seqlen_q, int max_seqlen_k, int total_q,
+                            int total_k, int dtype, int hq, int hkv, int d, float scale,
+                            int causal, int win_l, int win_r, float softcap,
+                            attn_stream_t stream);
+
+size_t attn_bwd_varlen_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
+                                      int total_q, int total_k, int hq, int hkv, int d,
+                                      int deterministic);
+
+attn_status attn_bwd_varlen(const void *q, const void *k, const void *v, const void *out,
+                            const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                            const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                            int batch, int max_seqlen_q, int max_seqlen_k, int total_q,
+                            int total_k, int dtype, int hq, int hkv, int d, float scale,
+                            int causal, int win_l, int win_r, float softcap, int deterministic,
+                            void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * Decode against a KV cache, with optional append (Inference Cookbook FAQ
+ * Q17, Q18, Q14).
+ *
+ * Paged (block_table != NULL): k_cache/v_cache are a page pool
+ * (num_pages, page_size, hkv, d); logical position t of batch entry i lives
+ * in page block_table[i*max_pages_per_seq + t/page_size], slot t%page_size.
+ * page_size must be a multiple of 128.  Contiguous (block_table == NULL):
+ * k_cache/v_cache are (b, page_size, hkv, d) -- one "page" of page_size
+ * tokens per batch entry; pass num_pages = b and max_pages_per_seq = 1.
+ *
+ * cache_seqlens (b) int32 DEVICE array: tokens already in the cache.  It is
+ * read, never written: the caller advances it by s_new after the call (FAQ
+ * Q17).  k_new/v_new (b, s_new, hkv, d), or NULL with s_new = 0: rows written
+ * into the cache at positions cache_seqlens[i] .. cache_seqlens[i]+s_new-1,
+ * and attended to.  Batch entry i attends over L_i = cache_seqlens[i] + s_new
+ * keys with the bottom-right mask (query r sits at position L_i - sq + r).
+ * Every L_i must fit max_pages_per_seq * page_size; the block_table entries
+ * used must lie in [0, num_pages) (checked on the device: the device error
+ * word is raised and the entry's output is left unwritten).
+ *
+ * q (b,sq,hq,d), out (b,sq,hq,d), lse (b,hq,sq) fp32.
+ *
+ * num_splits: 0 = choose from the SM count and the cache length (FAQ Q14),
+ * else the number of key ranges each (batch, KV head) is split into; the
+ * split results are merged by their LSE.  workspace: at least
+ * attn_kvcache_workspace_size(...) bytes (may be 0 when one split is used).
+ */
+int attn_kvcache_num_splits(int b, int sq, int hq, int hkv, int d, int max_seqlen_k,
+                            int num_splits);
+
+size_t attn_kvcache_workspace_size(int b, int sq, int hq, int hkv, int d, int max_seqlen_k,
+                                   int num_splits);
+
+attn_status attn_fwd_kvcache(const void *q, void *k_cache, void *v_cache, const void *k_new,
+                             const void *v_new, const int32_t *cache_seqlens,
+                             const int32_t *block_table, int num_pages, int page_size,
+                             int max_pages_per_seq, void *out, float *lse, int dtype, int b,
+                             int sq, int s_new, int hq, int hkv, int d, float scale, int causal,
+                             int win_l, int win_r, float softcap, int num_splits,
+                             void *workspace, size_t workspace_bytes, attn_stream_t stream);
+
+/*
+ * Reads and clears the sticky device error word of the current device
+ * (synchronises `stream`; diagnostic use, not for the hot path).  Returns
+ * ATTN_OK, ATTN_ERR_DEVICE or ATTN_ERR_TIMEOUT.  If `detail` is not NULL it
+ * receives the raw error word (which check fired).
+ */
+attn_status attn_get_device_error(attn_stream_t stream, int *detail);
+
+/*
+ * Number of kernels this library has enqueued since it was loaded (all
+ * devices and threads; a relaxed atomic counter).  Lets a caller count the
+ * library's launches inside a timed region.  Host only.
+ */
+unsigned long long attn_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBATTN_H */

@@ -1,0 +1,70 @@
+"""Backward parity (both dQ modes) against the float64 oracle."""
+import math
+
+import numpy as np
+import pytest
+
+from exact_attention_41_gb300 import synthetic as syn
+from oracle import attention as ref
+from tests.helpers import assert_close, dev, f64, host
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_fwd_bwd(case, dtype, deterministic, **kw):
+    from exact_attention_41_gb300 import libattn
+
+    q, k, v, do = (dev(case[x], dtype) for x in ("q", "k", "v", "dout"))
+    o, lse = libattn.fwd(q, k, v, **kw)
+    return libattn.bwd(q, k, v, o, lse, do, deterministic=deterministic, **kw)
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+@pytest.mark.parametrize("dtype", [syn.F16, syn.BF16])
+@pytest.mark.parametrize("kw", [
+    dict(),
+    dict(causal=True),
+    dict(causal=True, window=(40, 0), softcap=5.0),
+    dict(window=(7, 19)),
+])
+@pytest.mark.parametrize("shape", [(2, 256, 256, 4, 2, 128), (1, 193, 67, 4, 1, 64),
+                                   (1, 67, 193, 2, 2, 256), (2, 130, 130, 8, 8, 128)])
+def test_small_full(deterministic, dtype, kw, shape):
+    b, sq, sk, hq, hkv, d = shape
+    case = syn.dense_case(21, b, sq, sk, hq, hkv, d, dtype, with_dout=True)
+    dq, dk, dv = gpu_fwd_bwd(case, dtype, deterministic, **kw)
+    scale = 1 / math.sqrt(d)
+    win = kw.get("window", (-1, -1))
+    rq, rk, rv = ref.backward(*(f64(case[x], dtype) for x in ("q", "k", "v", "dout")), scale,
+                              kw.get("causal", False), win[0], win[1], kw.get("softcap", 0.0))
+    assert_close(host(dq), rq, dtype, "dq")
+    assert_close(host(dk), rk, dtype, "dk")
+    assert_close(host(dv), rv, dtype, "dv")
+
+
+def test_deterministic_is_bitwise_repeatable():
+    case = syn.dense_case(22, 2, 1024, 1024, 8, 2, 128, syn.BF16, with_dout=True)
+    a = gpu_fwd_bwd(case, syn.BF16, True, causal=True)
+    b = gpu_fwd_bwd(case, syn.BF16, True, causal=True)
+    import torch
+
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16), y.view(torch.int16))
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_training_shape_sampled_groups(deterministic):
+    """bf16 b=4, s=8192, hq=32, hkv=8, d=128, causal; two seeded (b, kv head)
+    groups checked in full: the group's dQ rows and that KV head's dK/dV."""
+    b, s, hq, hkv, d = 4, 8192, 32, 8, 128
+    g = hq // hkv
+    case = syn.dense_case(6, b, s, s, hq, hkv, d, syn.BF16, with_dout=True)
+    dq, dk, dv = gpu_fwd_bwd(case, syn.BF16, deterministic, causal=True)
+    q, k, v, do = (f64(case[x], syn.BF16) for x in ("q", "k", "v", "dout"))
+    rng = np.random.default_rng(601)
+    for _ in range(2):
+        bi, kv = int(rng.integers(b)), int(rng.integers(hkv))
+        rq, rk, rv = ref.backward_group(q, k, v, do, bi, kv, 1 / math.sqrt(d), causal=True)
+        assert_close(host(dq[bi, :, kv * g:(kv + 1) * g]), rq, syn.BF16, "dq")
+        assert_close(host(dk[bi, :, kv]), rk, syn.BF16, "dk")
+        assert_close(host(dv[bi, :, kv]), rv, syn.BF16, "dv")
