@@ -121,9 +121,9 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *out, flo
     return ATTN_ERR_UNSUPPORTED;
   const DeviceInfo *di = device_info();
   if (!di) return ATTN_ERR_CUDA;
-  FwdArgs a{q, k, v, out, lse, Seqs{nullptr, nullptr, sq, sk, 0, hq}, b, hq, hkv, d, dtype,
+  FwdArgs a{q, k, v, out, lse, Seqs{nullptr, nullptr, sq, sk, 0, 0, hq}, b, hq, hkv, d, dtype,
             scale, softcap > 0.f ? softcap : 0.f, win_l, win_r, di->err};
-  return launched(launch_fwd_simt(a, stream));
+  return launched(launch_fwd_tc(a, stream));
 }
 
 size_t attn_bwd_workspace_size(int b, int sq, int sk, int hq, int hkv, int d, int deterministic) {
@@ -156,7 +156,7 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *ou
   float *dsum = reinterpret_cast<float *>(ws);
   float *dq_acc = reinterpret_cast<float *>(ws + align256(sizeof(float) * (size_t)b * sq * hq));
   BwdArgs a{FwdArgs{q, k, v, const_cast<void *>(out), const_cast<float *>(lse),
-                    Seqs{nullptr, nullptr, sq, sk, 0, hq}, b, hq, hkv, d, dtype, scale,
+                    Seqs{nullptr, nullptr, sq, sk, 0, 0, hq}, b, hq, hkv, d, dtype, scale,
                     softcap > 0.f ? softcap : 0.f, win_l, win_r, di->err},
             dout, dq, dk, dv, dsum, dq_acc, deterministic};
   return launched(launch_bwd_simt(a, stream));
@@ -182,10 +182,10 @@ attn_status attn_fwd_varlen(const void *q, const void *k, const void *v, void *o
   const DeviceInfo *di = device_info();
   if (!di) return ATTN_ERR_CUDA;
   FwdArgs a{q, k, v, out, lse,
-            Seqs{cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, total_q, hq},
+            Seqs{cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, total_q, total_k, hq},
             batch, hq, hkv, d, dtype, scale, softcap > 0.f ? softcap : 0.f, win_l, win_r,
             di->err};
-  return launched(launch_fwd_simt(a, stream));
+  return launched(launch_fwd_tc(a, stream));
 }
 
 size_t attn_bwd_varlen_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
@@ -226,7 +226,7 @@ attn_status attn_bwd_varlen(const void *q, const void *k, const void *v, const v
   float *dsum = reinterpret_cast<float *>(ws);
   float *dq_acc = reinterpret_cast<float *>(ws + align256(sizeof(float) * (size_t)total_q * hq));
   BwdArgs a{FwdArgs{q, k, v, const_cast<void *>(out), const_cast<float *>(lse),
-                    Seqs{cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, total_q, hq},
+                    Seqs{cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, total_q, total_k, hq},
                     batch, hq, hkv, d, dtype, scale, softcap > 0.f ? softcap : 0.f, win_l, win_r,
                     di->err},
             dout, dq, dk, dv, dsum, dq_acc, deterministic};

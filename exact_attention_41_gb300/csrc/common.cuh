@@ -106,6 +106,7 @@ struct Seqs {
   const int32_t *cu_k;
   int sq, sk;           // dense lengths, or the stated maxima for varlen
   int total_q;          // varlen LSE row stride (hq, total_q); dense: unused
+  int total_k;          // varlen key rows; dense: unused
   int hq;
 
   // Returns false if the sequence is malformed (and raises the error word).

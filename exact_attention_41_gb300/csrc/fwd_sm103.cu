@@ -1,0 +1,413 @@
+// Forward attention on the 5th-generation tensor cores (sm_103a).
+//
+// One CTA owns one 128-row query tile of one (batch, head) and streams the
+// key/value tiles it may see ("FlashAttention完整说明" §二.1: tiling plus an
+// online softmax, so S and P never reach global memory).  Roles:
+//
+//   warp 0      TMA producer: Q once, then K and V tiles into a smem ring.
+//   warp 1      MMA issuer (one elected lane): S_j = Q K_j^T into TMEM,
+//               O += P_j V_j with P_j read from TMEM; also owns the TMEM
+//               allocation.
+//   warps 2-5   softmax warpgroup, one thread per query row: loads S_j from
+//               TMEM, applies scale -> softcap -> mask (Inference Cookbook
+//               FAQ Q22 order; bottom-right causal FAQ Q6; window FAQ Q21),
+//               runs the online max/sum update, writes P_j (fp16/bf16) back
+//               into the S_j columns, rescales O in TMEM when the running max
+//               grows by more than 2^8, and finally writes O / l and the LSE.
+//
+// TMEM (512 columns): O at [0, D), two S/P buffers at [D, D+BN) and
+// [D+BN, D+2BN), so S_{j+1} is computed while the softmax works on S_j.
+// The CTA order puts the heaviest causal query tiles first (longest job
+// first) and keeps the query heads of one KV head adjacent, so their K/V
+// tiles are shared through L2.
+#include <cudaTypedefs.h>
+
+#include "kernels.h"
+#include "sm103.cuh"
+
+namespace attn {
+namespace {
+using namespace sm103;
+
+constexpr int kBM = 128;
+constexpr int kThreads = 192;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when max grows > 256x
+
+template <int D, int BN>
+struct FwdCfg {
+  static constexpr int kStages = (D == 64) ? 3 : 2;
+  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kKVBytes = BN * D * 2;
+  static constexpr int kSmemData = kQBytes + 2 * kStages * kKVBytes;
+  // at least ~120 KB so that one CTA owns the SM (and all 512 TMEM columns)
+  static constexpr int kSmem = (kSmemData + 1024 > 120 * 1024 ? kSmemData + 1024 : 120 * 1024);
+  static constexpr int kSCol0 = D;
+  static constexpr uint32_t kTmemCols = 512;
+};
+
+struct Shared {
+  uint64_t q_full;
+  uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
+  uint64_t s_full[2], p_full[2], o_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_bar(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_test(a, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t spin = 1;; ++spin) {
+    if (mbar_test(a, parity)) return true;
+    if ((spin & 255) == 0) {
+      if (*(volatile int *)&sh.abort) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        raise_error(err, kErrTimeout);
+        *(volatile int *)&sh.abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+template <typename T> struct IsBf16 { static constexpr int v = 0; };
+template <> struct IsBf16<__nv_bfloat16> { static constexpr int v = 1; };
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float a, float b) { return Elem<T>::from_f2(a, b); }
+
+template <typename T, int D, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const FwdArgs a, const int m_blocks) {
+  using C = FwdCfg<D, BN>;
+  constexpr int ST = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Shared sh;
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint8_t *q_s = smem;
+  uint8_t *k_s = smem + C::kQBytes;
+  uint8_t *v_s = k_s + ST * C::kKVBytes;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTA -> (query tile, batch, head): heaviest tiles first, heads fastest.
+  const int bid = blockIdx.x;
+  const int h = bid % a.hq;
+  const int b = (bid / a.hq) % a.batch;
+  const int mb = m_blocks - 1 - bid / (a.hq * a.batch);
+  int q0, lq, k0, lk;
+  if (!a.seqs.get(b, q0, lq, k0, lk, a.err)) return;
+  const int m0 = mb * kBM;
+  if (m0 >= lq) return;
+  const int kvh = h / (a.hq / a.hkv);
+  const int m_last = min(m0 + kBM, lq) - 1;
+
+  // key tiles any row of this query tile may see
+  int lo_first, hi_first, lo_last, hi_last;
+  key_range(m0, lq, lk, a.win_l, a.win_r, lo_first, hi_first);
+  key_range(m_last, lq, lk, a.win_l, a.win_r, lo_last, hi_last);
+  int n_lo = 0, nt = 0;
+  if (hi_last >= lo_first && hi_last >= 0) {
+    n_lo = lo_first / BN;
+    nt = hi_last / BN - n_lo + 1;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sh.q_full, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&sh.k_full[s], 1);
+      mbar_init(&sh.k_empty[s], 1);
+      mbar_init(&sh.v_full[s], 1);
+      mbar_init(&sh.v_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sh.s_full[s], 1);
+      mbar_init(&sh.p_full[s], kBM);
+    }
+    mbar_init(&sh.o_done, 1);
+    sh.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one()) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      mbar_expect_tx(&sh.q_full, C::kQBytes);
+      for (int c = 0; c < D / 64; ++c)
+        tma_load_3d(q_s + c * kBM * 128, &tq, &sh.q_full, c * 64, h, q0 + m0);
+      int issued = 0;
+      for (int j = 0; j < nt; ++j) {
+        const int st = j % ST;
+        const uint32_t ph = (j / ST) & 1;
+        const int krow = k0 + (n_lo + j) * BN;
+        if (!wait_bar(sh, &sh.k_empty[st], ph ^ 1, a.err)) break;
+        mbar_expect_tx(&sh.k_full[st], C::kKVBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(k_s + st * C::kKVBytes + c * BN * 128, &tk, &sh.k_full[st], c * 64, kvh,
+                      krow);
+        if (!wait_bar(sh, &sh.v_empty[st], ph ^ 1, a.err)) { issued = 2 * j + 1; break; }
+        mbar_expect_tx(&sh.v_full[st], C::kKVBytes);
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(v_s + st * C::kKVBytes + c * BN * 128, &tv, &sh.v_full[st], c * 64, kvh,
+                      krow);
+        issued = 2 * j + 2;
+      }
+      if (*(volatile int *)&sh.abort) {
+        // let this CTA's copies in flight land before the CTA exits
+        int *noerr = nullptr;
+        mbar_wait(&sh.q_full, 0, noerr);
+        for (int x = max(0, issued - 2 * ST); x < issued; ++x) {
+          const int j = x / 2, st = j % ST;
+          mbar_wait(x % 2 ? &sh.v_full[st] : &sh.k_full[st], (j / ST) & 1, noerr);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      constexpr int ab = IsBf16<T>::v;
+      constexpr uint32_t id_s = idesc_f16(kBM, BN, ab, 0, 0);
+      constexpr uint32_t id_o = idesc_f16(kBM, D, ab, 0, 1);
+      const uint32_t q_addr = smem_u32(q_s), k_addr = smem_u32(k_s), v_addr = smem_u32(v_s);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j % ST;
+        if (!wait_bar(sh, &sh.k_full[st], (j / ST) & 1, a.err)) return false;
+        tc_fence_after();
+        const uint32_t dcol = tmem + C::kSCol0 + (j & 1) * BN;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t ad = smem_desc(q_addr + (kk / 4) * (kBM * 128) + (kk % 4) * 32, 16, 1024);
+          const uint64_t bd = smem_desc(k_addr + st * C::kKVBytes + (kk / 4) * (BN * 128) +
+                                            (kk % 4) * 32, 16, 1024);
+          mma_ss(dcol, ad, bd, id_s, kk > 0);
+        }
+        mma_commit(&sh.s_full[j & 1]);
+        mma_commit(&sh.k_empty[st]);
+        return true;
+      };
+      bool ok = nt == 0 || (wait_bar(sh, &sh.q_full, 0, a.err) && issue_s(0));
+      for (int j = 0; ok && j < nt; ++j) {
+        if (j + 1 < nt && !issue_s(j + 1)) break;
+        if (!wait_bar(sh, &sh.p_full[j & 1], (j >> 1) & 1, a.err)) break;
+        const int st = j % ST;
+        if (!wait_bar(sh, &sh.v_full[st], (j / ST) & 1, a.err)) break;
+        tc_fence_after();
+        const uint32_t pcol = tmem + C::kSCol0 + (j & 1) * BN;
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          const uint64_t bd = smem_desc(v_addr + st * C::kKVBytes + kk * 16 * 128, BN * 128, 1024);
+          mma_ts(tmem, pcol + kk * 8, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&sh.o_done);
+        mma_commit(&sh.v_empty[st]);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int r = 32 * (warp & 3) + lane;  // TMEM lane = query row in the tile
+    const int i = m0 + r;
+    const uint32_t row_t = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    int lo_i, hi_i;
+    key_range(i, lq, lk, a.win_l, a.win_r, lo_i, hi_i);
+    // tiles that need no mask: every row of the tile sees every key in them
+    int lo_tile_max, hi_tile_min, dummy;
+    key_range(m0 + kBM - 1, lq, lk, a.win_l, a.win_r, lo_tile_max, dummy);
+    key_range(m0, lq, lk, a.win_l, a.win_r, dummy, hi_tile_min);
+    const float sl2 = a.scale * kLog2e;
+    const bool cap = a.softcap > 0.f;
+    const float cap_in = cap ? a.scale / a.softcap : 0.f, cap_out = a.softcap * kLog2e;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < nt; ++j) {
+      const int key0 = (n_lo + j) * BN;
+      if (!wait_bar(sh, &sh.s_full[j & 1], (j >> 1) & 1, a.err)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t scol = row_t + C::kSCol0 + (j & 1) * BN;
+      float x[BN];
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t u[32];
+        tmem_ld32(scol + c * 32, u);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(u[e]);
+      }
+      const bool need_mask = key0 < lo_tile_max || key0 + BN - 1 > hi_tile_min;
+      float mt = -INFINITY;
+#pragma unroll
+      for (int e = 0; e < BN; ++e) {
+        float v = cap ? cap_out * tanhf(x[e] * cap_in) : x[e] * sl2;
+        if (need_mask) {
+          const int kj = key0 + e;
+          if (kj < lo_i || kj > hi_i) v = -INFINITY;
+        }
+        x[e] = v;
+        mt = fmaxf(mt, v);
+      }
+      const float m_new = fmaxf(m_ref, mt);
+      const bool rescale = m_new > m_ref + kRescaleThreshold;
+      float alpha = 1.f;
+      if (rescale) {
+        alpha = ex2(m_ref - m_new);
+        l *= alpha;
+        m_ref = m_new;
+      }
+      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float p0 = ex2(x[c * 32 + 2 * e] - m_use);
+          const float p1 = ex2(x[c * 32 + 2 * e + 1] - m_use);
+          rs += p0 + p1;
+          pk[e] = pack2<T>(p0, p1);
+        }
+        tmem_st16(scol + c * 16, pk);
+      }
+      l += rs;
+      tmem_wait_st();
+      if (j > 0) {
+        // O holds P_{j-1} V_{j-1} once this completes; only then may it be rescaled
+        if (!wait_bar(sh, &sh.o_done, (j - 1) & 1, a.err)) { ok = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld32(row_t + c * 32, u);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
+            tmem_st32(row_t + c * 32, u);
+          }
+          tmem_wait_st();
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&sh.p_full[j & 1]);
+    }
+    // epilogue: O / l -> dtype, LSE = ln(sum exp(s))
+    if (ok && nt > 0) ok = wait_bar(sh, &sh.o_done, (nt - 1) & 1, a.err);
+    tc_fence_after();
+    if (ok) {
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      T *orow = static_cast<T *>(a.o) + ((int64_t)(q0 + i) * a.hq + h) * D;
+      const bool valid = i < lq;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t u[32];
+        if (nt > 0) {
+          tmem_ld32(row_t + c * 32, u);
+          tmem_wait_ld();
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) u[e] = 0u;
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack2<T>(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
+        if (valid) {
+          uint4 *dst = reinterpret_cast<uint4 *>(orow + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        }
+      }
+      if (valid) {
+        const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+        a.lse[a.seqs.lse_index(b, h, q0, i)] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// (rows, heads, D) tensor, box {64, 1, box_rows}, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const void *base, int dtype, int64_t rows, int heads, int d,
+              int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+             3, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <typename T, int D, int BN>
+cudaError_t fwd_tc(const FwdArgs &a, cudaStream_t st) {
+  using C = FwdCfg<D, BN>;
+  const int64_t rows_q = a.seqs.cu_q ? a.seqs.total_q : (int64_t)a.batch * a.seqs.sq;
+  const int64_t rows_k = a.seqs.cu_k ? a.seqs.total_k : (int64_t)a.batch * a.seqs.sk;
+  if (rows_k == 0) return launch_fwd_simt(a, st);  // no keys: every row is empty
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, a.q, a.dtype, rows_q, a.hq, D, kBM) ||
+      !make_map(&tk, a.k, a.dtype, rows_k, a.hkv, D, BN) ||
+      !make_map(&tv, a.v, a.dtype, rows_k, a.hkv, D, BN))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<T, D, BN>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  const int m_blocks = (a.seqs.sq + kBM - 1) / kBM;
+  const int64_t grid = (int64_t)m_blocks * a.hq * a.batch;
+  if (grid == 0) return cudaSuccess;
+  if (grid > INT32_MAX) return cudaErrorInvalidValue;
+  fwd_tc_kernel<T, D, BN><<<(unsigned)grid, kThreads, C::kSmem, st>>>(tq, tk, tv, a, m_blocks);
+  count_launches(1);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t st) {
+  const bool bf = a.dtype == ATTN_BF16;
+  switch (a.d) {
+    case 64: return bf ? fwd_tc<__nv_bfloat16, 64, 128>(a, st) : fwd_tc<__half, 64, 128>(a, st);
+    case 128: return bf ? fwd_tc<__nv_bfloat16, 128, 128>(a, st) : fwd_tc<__half, 128, 128>(a, st);
+    case 256: return bf ? fwd_tc<__nv_bfloat16, 256, 64>(a, st) : fwd_tc<__half, 256, 64>(a, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace attn

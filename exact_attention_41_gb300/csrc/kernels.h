@@ -47,6 +47,7 @@ struct DecodeArgs {
 void count_launches(int n);
 
 cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t st);
+cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t st);
 cudaError_t launch_bwd_simt(const BwdArgs &a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
 

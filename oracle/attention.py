@@ -144,21 +144,44 @@ def forward_rows(q, k, v, samples, scale, causal=False, win_l=-1, win_r=-1, soft
     return o, lse
 
 
+def round_to(x, dtype):
+    """Round float64 values to fp16 or bf16 (round to nearest even), as the
+    forward's stored output is; returns float64."""
+    if dtype == "f16":
+        return x.astype(np.float16).astype(np.float64)
+    if dtype == "bf16":
+        f = x.astype(np.float32)
+        u = f.view(np.uint32).astype(np.uint64)
+        u = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16) << 16
+        return u.astype(np.uint32).view(np.float32).astype(np.float64)
+    raise ValueError(dtype)
+
+
 def head_backward(qh, kh, vh, doh, sq, sk, scale, causal=False, win_l=-1, win_r=-1,
-                  softcap=0.0):
+                  softcap=0.0, stored_o=None):
     """Gradients of one (batch, head) problem.  Returns dq (sq,d), dk (sk,d), dv (sk,d).
 
     P is recomputed from Q and K (FlashAttention完整说明 section 二.2); then
       dV = P^T dO,  dP = dO V^T,  D_i = sum_j P_ij dP_ij,
       dS = P * (dP - D)  [* (1 - tanh(s_raw/c)^2) with softcap c],
       dQ = scale * dS K,  dK = scale * dS^T Q.
+
+    stored_o: None gives the exact gradient.  "f16"/"bf16" instead takes
+    D_i = dO_i . O_i with O_i the forward output rounded to that storage type,
+    i.e. the output the forward saves (same page, section 二.2: the forward
+    keeps only O and the softmax statistics for the backward).  The two
+    differ only by that rounding; D_i = dO_i . O_i holds exactly since the
+    rows of P sum to one.
     """
     s, s_raw = _scores(qh, kh, scale, softcap)
     mask = visible(np.arange(sq), sq, sk, causal, win_l, win_r)
     p, _ = _softmax_rows(s, mask)
     dv = p.T @ doh
     dp = doh @ vh.T
-    dsum = (p * dp).sum(axis=1)
+    if stored_o is None:
+        dsum = (p * dp).sum(axis=1)
+    else:
+        dsum = (doh * round_to(p @ vh, stored_o)).sum(axis=1)
     ds = p * (dp - dsum[:, None])
     if softcap > 0:
         ds = ds * (1.0 - np.tanh(s_raw / softcap) ** 2)
@@ -168,7 +191,7 @@ def head_backward(qh, kh, vh, doh, sq, sk, scale, causal=False, win_l=-1, win_r=
 
 
 def backward_group(q, k, v, dout, bi, kv, scale, causal=False, win_l=-1, win_r=-1,
-                   softcap=0.0):
+                   softcap=0.0, stored_o=None):
     """Gradients restricted to one (batch, KV head) group.
 
     Returns dq (sq, g, d) for the group's query heads h = kv*g .. kv*g+g-1,
@@ -183,14 +206,15 @@ def backward_group(q, k, v, dout, bi, kv, scale, causal=False, win_l=-1, win_r=-
     for t in range(g):
         h = kv * g + t
         a, bk, bv = head_backward(q[bi, :, h], k[bi, :, kv], v[bi, :, kv], dout[bi, :, h],
-                                  sq, sk, scale, causal, win_l, win_r, softcap)
+                                  sq, sk, scale, causal, win_l, win_r, softcap, stored_o)
         dq[:, t] = a
         dk += bk
         dv += bv
     return dq, dk, dv
 
 
-def backward(q, k, v, dout, scale, causal=False, win_l=-1, win_r=-1, softcap=0.0):
+def backward(q, k, v, dout, scale, causal=False, win_l=-1, win_r=-1, softcap=0.0,
+             stored_o=None):
     """Dense gradients dq (b,sq,hq,d), dk/dv (b,sk,hkv,d) in float64."""
     b, sq, hq, d = q.shape
     sk, hkv = k.shape[1], k.shape[2]
@@ -201,7 +225,7 @@ def backward(q, k, v, dout, scale, causal=False, win_l=-1, win_r=-1, softcap=0.0
     for bi in range(b):
         for kv in range(hkv):
             a, bk, bv = backward_group(q, k, v, dout, bi, kv, scale, causal, win_l, win_r,
-                                       softcap)
+                                       softcap, stored_o)
             dq[bi, :, kv * g:(kv + 1) * g] = a
             dk[bi, :, kv] = bk
             dv[bi, :, kv] = bv
@@ -230,7 +254,7 @@ def varlen_forward(q, k, v, cu_q, cu_k, scale, causal=False, win_l=-1, win_r=-1,
 
 
 def varlen_backward(q, k, v, dout, cu_q, cu_k, scale, causal=False, win_l=-1, win_r=-1,
-                    softcap=0.0, seqs=None):
+                    softcap=0.0, seqs=None, stored_o=None):
     """Packed varlen gradients; sequences not in ``seqs`` are left as NaN."""
     dq = np.full(q.shape, np.nan)
     dk = np.full(k.shape, np.nan)
@@ -239,7 +263,7 @@ def varlen_backward(q, k, v, dout, cu_q, cu_k, scale, causal=False, win_l=-1, wi
     for i in (range(nseq) if seqs is None else seqs):
         q0, q1, k0, k1 = int(cu_q[i]), int(cu_q[i + 1]), int(cu_k[i]), int(cu_k[i + 1])
         a, bk, bv = backward(q[None, q0:q1], k[None, k0:k1], v[None, k0:k1],
-                             dout[None, q0:q1], scale, causal, win_l, win_r, softcap)
+                             dout[None, q0:q1], scale, causal, win_l, win_r, softcap, stored_o)
         dq[q0:q1], dk[k0:k1], dv[k0:k1] = a[0], bk[0], bv[0]
     return dq, dk, dv
 

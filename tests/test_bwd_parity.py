@@ -1,4 +1,7 @@
-"""Backward parity (both dQ modes) against the float64 oracle."""
+"""Backward parity (both dQ modes) against the float64 oracle.
+
+The oracle's D_i is taken from the stored (rounded) forward output, as the
+backward on the pages recomputes from the saved O (oracle ``stored_o``)."""
 import math
 
 import numpy as np
@@ -36,7 +39,8 @@ def test_small_full(deterministic, dtype, kw, shape):
     scale = 1 / math.sqrt(d)
     win = kw.get("window", (-1, -1))
     rq, rk, rv = ref.backward(*(f64(case[x], dtype) for x in ("q", "k", "v", "dout")), scale,
-                              kw.get("causal", False), win[0], win[1], kw.get("softcap", 0.0))
+                              kw.get("causal", False), win[0], win[1], kw.get("softcap", 0.0),
+                              stored_o=dtype)
     assert_close(host(dq), rq, dtype, "dq")
     assert_close(host(dk), rk, dtype, "dk")
     assert_close(host(dv), rv, dtype, "dv")
@@ -64,7 +68,8 @@ def test_training_shape_sampled_groups(deterministic):
     rng = np.random.default_rng(601)
     for _ in range(2):
         bi, kv = int(rng.integers(b)), int(rng.integers(hkv))
-        rq, rk, rv = ref.backward_group(q, k, v, do, bi, kv, 1 / math.sqrt(d), causal=True)
+        rq, rk, rv = ref.backward_group(q, k, v, do, bi, kv, 1 / math.sqrt(d), causal=True,
+                                        stored_o=syn.BF16)
         assert_close(host(dq[bi, :, kv * g:(kv + 1) * g]), rq, syn.BF16, "dq")
         assert_close(host(dk[bi, :, kv]), rk, syn.BF16, "dk")
         assert_close(host(dv[bi, :, kv]), rv, syn.BF16, "dv")

@@ -401,3 +401,19 @@ def test_output_shape_is_query_shape():
         q = rnd(60, *small)
         o, lse = ref.forward(q, q.copy(), q.copy(), 1.0)
         assert o.shape == small and lse.shape == (small[0], small[2], small[1])
+
+
+def test_stored_output_reading_of_d():
+    """D_i from the stored (rounded) O: with the exact O it is the textbook
+    D_i = sum_j P_ij dP_ij (rows of P sum to one); with O rounded the
+    gradients move by no more than the rounding allows."""
+    q, k, v, do = rnd(62, 1, 9, 2, 8), rnd(63, 1, 11, 1, 8), rnd(64, 1, 11, 1, 8), rnd(65, 1, 9, 2, 8)
+    exact = ref.backward(q, k, v, do, 0.4, causal=True)
+    for dt in ("bf16", "f16"):
+        got = ref.backward(q, k, v, do, 0.4, causal=True, stored_o=dt)
+        np.testing.assert_array_equal(got[2], exact[2])  # dV does not involve D
+        eps = 2.0 ** (-8 if dt == "bf16" else -11)
+        assert np.abs(got[0] - exact[0]).max() < 50 * eps
+        assert np.abs(got[0] - exact[0]).max() > 0
+    np.testing.assert_array_equal(ref.round_to(np.array([1.0, 1.00390625, 1.01171875]), "bf16"),
+                                  [1.0, 1.0, 1.015625])

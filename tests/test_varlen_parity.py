@@ -40,7 +40,7 @@ def test_small_packed(dtype, kw):
     ro, rl = ref.varlen_forward(*args, *a)
     assert_close(host(o), ro, dtype, "out")
     assert_lse(host(lse), rl)
-    rq, rk, rv = ref.varlen_backward(*args, f64(case["dout"], dtype), *a)
+    rq, rk, rv = ref.varlen_backward(*args, f64(case["dout"], dtype), *a, stored_o=dtype)
     assert_close(host(dq), rq, dtype, "dq")
     assert_close(host(dk), rk, dtype, "dk")
     assert_close(host(dv), rv, dtype, "dv")
@@ -59,7 +59,8 @@ def test_workload_sampled_sequences(deterministic):
     args = [f64(case[x], syn.BF16) for x in ("q", "k", "v")]
     a = (case["cu_seqlens_q"], case["cu_seqlens_k"], 1 / math.sqrt(128), True, 256, 0, 50.0)
     ro, rl = ref.varlen_forward(*args, *a, seqs=seqs)
-    rq, rk, rv = ref.varlen_backward(*args, f64(case["dout"], syn.BF16), *a, seqs=seqs)
+    rq, rk, rv = ref.varlen_backward(*args, f64(case["dout"], syn.BF16), *a, seqs=seqs,
+                                     stored_o=syn.BF16)
     cu = case["cu_seqlens_q"]
     rows = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in seqs])
     assert_close(host(o)[rows], ro[rows], syn.BF16, "out")
