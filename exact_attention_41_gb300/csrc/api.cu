@@ -60,11 +60,30 @@ attn_status check_common(int dtype, int hq, int hkv, int d, float scale, int win
 
 attn_status launched(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
-// Bytes of the backward workspace for `rows` query rows in total.
-size_t bwd_ws_bytes(int64_t rows, int hq, int d, int64_t mblocks) {
-  return align256(sizeof(float) * rows * hq)            // D_i
-         + align256(sizeof(float) * rows * hq * d)      // fp32 dQ accumulator
-         + align256(sizeof(int) * (mblocks + 1) * hq);  // ordering counters
+// Turn counters per query head: one per 64-row query chunk of every
+// sequence (chunk c of sequence b at index cu_q[b]/64 + b + c).
+int64_t sem_per_head(int64_t rows, int batch) { return rows / 64 + batch + 1; }
+
+// Backward workspace for `rows` query rows in total: D_i (fp32, LSE
+// layout), the fp32 dQ accumulator, and the turn counters.
+size_t bwd_ws_bytes(int64_t rows, int hq, int d, int batch) {
+  return align256(sizeof(float) * rows * hq) + align256(sizeof(float) * rows * hq * d) +
+         align256(sizeof(int) * sem_per_head(rows, batch) * hq);
+}
+
+// Splits a backward workspace and launches the backward kernels.
+attn_status run_bwd(BwdArgs &a, int64_t rows, void *workspace, const DeviceInfo *di,
+                    cudaStream_t stream) {
+  char *ws = static_cast<char *>(workspace);
+  const int hq = a.f.hq;
+  a.dsum = reinterpret_cast<float *>(ws);
+  ws += align256(sizeof(float) * rows * hq);
+  a.dq_acc = reinterpret_cast<float *>(ws);
+  ws += align256(sizeof(float) * rows * hq * a.f.d);
+  int *sem = reinterpret_cast<int *>(ws);
+  if (a.f.d == 128)
+    return launched(launch_bwd_tc(a, sem, (int)sem_per_head(rows, a.f.batch), di->sms, stream));
+  return launched(launch_bwd_simt(a, stream));
 }
 
 int resolve_splits(int b, int hkv, int max_seqlen_k, int num_splits, int sms) {
@@ -129,7 +148,7 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *out, flo
 size_t attn_bwd_workspace_size(int b, int sq, int sk, int hq, int hkv, int d, int deterministic) {
   (void)sk; (void)hkv; (void)deterministic;
   if (b <= 0 || sq <= 0 || hq <= 0 || d <= 0) return 0;
-  return bwd_ws_bytes((int64_t)b * sq, hq, d, (int64_t)b * ((sq + 127) / 128));
+  return bwd_ws_bytes((int64_t)b * sq, hq, d, b);
 }
 
 attn_status attn_bwd(const void *q, const void *k, const void *v, const void *out,
@@ -152,14 +171,11 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *ou
   if (need > 0 && (!workspace || workspace_bytes < need)) return ATTN_ERR_WORKSPACE;
   const DeviceInfo *di = device_info();
   if (!di) return ATTN_ERR_CUDA;
-  char *ws = static_cast<char *>(workspace);
-  float *dsum = reinterpret_cast<float *>(ws);
-  float *dq_acc = reinterpret_cast<float *>(ws + align256(sizeof(float) * (size_t)b * sq * hq));
   BwdArgs a{FwdArgs{q, k, v, const_cast<void *>(out), const_cast<float *>(lse),
                     Seqs{nullptr, nullptr, sq, sk, 0, 0, hq}, b, hq, hkv, d, dtype, scale,
                     softcap > 0.f ? softcap : 0.f, win_l, win_r, di->err},
-            dout, dq, dk, dv, dsum, dq_acc, deterministic};
-  return launched(launch_bwd_simt(a, stream));
+            dout, dq, dk, dv, nullptr, nullptr, deterministic};
+  return run_bwd(a, (int64_t)b * sq, workspace, di, stream);
 }
 
 attn_status attn_fwd_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
@@ -193,7 +209,7 @@ size_t attn_bwd_varlen_workspace_size(int batch, int max_seqlen_q, int max_seqle
                                       int deterministic) {
   (void)max_seqlen_q; (void)max_seqlen_k; (void)total_k; (void)hkv; (void)deterministic;
   if (batch <= 0 || total_q <= 0 || hq <= 0 || d <= 0) return 0;
-  return bwd_ws_bytes(total_q, hq, d, (int64_t)total_q / 128 + batch);
+  return bwd_ws_bytes(total_q, hq, d, batch);
 }
 
 attn_status attn_bwd_varlen(const void *q, const void *k, const void *v, const void *out,
@@ -222,15 +238,12 @@ attn_status attn_bwd_varlen(const void *q, const void *k, const void *v, const v
   if (need > 0 && (!workspace || workspace_bytes < need)) return ATTN_ERR_WORKSPACE;
   const DeviceInfo *di = device_info();
   if (!di) return ATTN_ERR_CUDA;
-  char *ws = static_cast<char *>(workspace);
-  float *dsum = reinterpret_cast<float *>(ws);
-  float *dq_acc = reinterpret_cast<float *>(ws + align256(sizeof(float) * (size_t)total_q * hq));
   BwdArgs a{FwdArgs{q, k, v, const_cast<void *>(out), const_cast<float *>(lse),
                     Seqs{cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, total_q, total_k, hq},
                     batch, hq, hkv, d, dtype, scale, softcap > 0.f ? softcap : 0.f, win_l, win_r,
                     di->err},
-            dout, dq, dk, dv, dsum, dq_acc, deterministic};
-  return launched(launch_bwd_simt(a, stream));
+            dout, dq, dk, dv, nullptr, nullptr, deterministic};
+  return run_bwd(a, total_q, workspace, di, stream);
 }
 
 int attn_kvcache_num_splits(int b, int sq, int hq, int hkv, int d, int max_seqlen_k,

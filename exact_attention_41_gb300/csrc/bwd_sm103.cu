@@ -1,0 +1,520 @@
+// Backward attention on the 5th-generation tensor cores (sm_103a), d = 128.
+//
+// "FlashAttention完整说明" §二.2: the forward keeps only O and the softmax
+// statistics; the backward recomputes S and P tile by tile from Q, K and the
+// saved LSE.  With D_i = sum_c dO_ic O_ic (the preprocess kernel):
+//
+//   P = exp(s - LSE),  dV += P^T dO,  dP = dO V^T,
+//   dS = P * (dP - D) [* (1 - tanh^2) under softcap],
+//   dK += dS^T Q,  dQ += dS K          (dK, dQ scaled by `scale` at the end)
+//
+// One CTA owns a block of 128 keys of one (batch, KV head) and loops over the
+// query heads of its GQA group and the 64-row query chunks that can see those
+// keys.  Roles:
+//
+//   warp 0      TMA producer: K and V once, Q and dO chunks into a 2-stage ring.
+//   warp 1      MMA issuer: S^T = K Q^T and dP^T = V dO^T into TMEM, then
+//               dV += P^T dO, dK += dS^T Q (P^T, dS^T from shared memory) and
+//               dQ^T = K^T dS^T into one of two TMEM buffers.
+//   warps 2-5   one thread per key row: P^T and dS^T from S^T, dP^T (TMEM),
+//               the chunk's LSE and D; bf16/fp16 into shared memory for the
+//               MMAs; finally dK and dV out of TMEM.
+//   warps 6-9   one thread per head-dim column: dQ^T out of TMEM, added into
+//               an fp32 dQ accumulator in global memory.  In deterministic
+//               mode the key blocks add to each query chunk in key-block order
+//               (a per-chunk turn counter), so the fp32 sums are bitwise
+//               reproducible (Inference Cookbook FAQ Q11).
+//
+// TMEM (512 columns): dV [0,128), dK [128,256), S^T [256,320), dP^T [320,384),
+// dQ^T buffers [384,448) and [448,512).
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+
+#include "kernels.h"
+#include "sm103.cuh"
+
+namespace attn {
+
+bool make_map_3d(CUtensorMap *m, const void *base, int dtype, int64_t rows, int heads, int d,
+                 int box_rows);
+
+namespace {
+using namespace sm103;
+
+constexpr int D = 128;
+constexpr int BN = 128;   // keys per CTA
+constexpr int BQ = 64;    // query rows per iteration
+constexpr int ST = 2;     // Q/dO ring stages
+constexpr int kThreads = 320;
+constexpr int kTileK = BN * D * 2;       // 32 KB
+constexpr int kChunk = BQ * D * 2;       // 16 KB
+constexpr int kPT = BN * BQ * 2;         // 16 KB
+constexpr int kSmemData = 2 * kTileK + ST * 2 * kChunk + 2 * 2 * kPT;  // 192 KB
+constexpr int kSmem = kSmemData + 1024;
+constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 320, kColDQ = 384;
+
+struct Shared {
+  uint64_t kv_full;
+  uint64_t qd_full[ST], qd_empty[ST];
+  uint64_t sdp_full, st_free;
+  uint64_t pds_full[2], mma_done[2], dq_free[2];
+  uint32_t tmem_base;
+  int abort;
+  float lse2[2][BQ];
+  float dsum[2][BQ];
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ bool wait_bar(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_test(a, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t spin = 1;; ++spin) {
+    if (mbar_test(a, parity)) return true;
+    if ((spin & 255) == 0) {
+      if (*(volatile int *)&sh.abort) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        raise_error(err, kErrTimeout);
+        *(volatile int *)&sh.abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
+template <typename T> struct IsBf16 { static constexpr int v = 0; };
+template <> struct IsBf16<__nv_bfloat16> { static constexpr int v = 1; };
+
+struct BwdGeom {
+  int q0, lq, k0, lk, key0, c_lo, nch, n_iter;
+};
+
+// Query chunks [c_lo, c_lo + nch) that can see any key of block nb.
+__device__ __forceinline__ void chunk_range(int nb, int lq, int lk, int win_l, int win_r,
+                                            int &c_lo, int &nch) {
+  const int key0 = nb * BN, key1 = min(key0 + BN, lk) - 1;
+  int lo0, hi0, lo1, hi1;
+  query_range(key0, lq, lk, win_l, win_r, lo0, hi0);
+  query_range(key1, lq, lk, win_l, win_r, lo1, hi1);
+  if (key1 < key0 || hi1 < lo0 || hi1 < 0 || lo0 > lq - 1) {
+    c_lo = 0;
+    nch = 0;
+    return;
+  }
+  c_lo = lo0 / BQ;
+  nch = hi1 / BQ - c_lo + 1;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                  const BwdArgs a, const int n_blocks, int *sem, const int sem_per_head) {
+  const FwdArgs &f = a.f;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Shared sh;
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                              ~uintptr_t(1023));
+  uint8_t *k_s = smem;
+  uint8_t *v_s = smem + kTileK;
+  uint8_t *qd_s = smem + 2 * kTileK;           // [stage][Q | dO]
+  uint8_t *pt_s = qd_s + ST * 2 * kChunk;      // [buf][P^T | dS^T]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTA -> (key block, kv head, batch): key blocks fastest, so the CTAs of one
+  // (batch, kv head) run together and share Q/dO in L2; lower key blocks (the
+  // heaviest under a causal mask) are dispatched first.
+  const int bid = blockIdx.x;
+  const int nb = bid % n_blocks;
+  const int kvh = (bid / n_blocks) % f.hkv;
+  const int b = bid / (n_blocks * f.hkv);
+  int q0, lq, k0, lk;
+  if (!f.seqs.get(b, q0, lq, k0, lk, f.err)) return;
+  const int key0 = nb * BN;
+  if (key0 >= lk) return;
+  const int g = f.hq / f.hkv;
+  int c_lo, nch;
+  chunk_range(nb, lq, lk, f.win_l, f.win_r, c_lo, nch);
+  const int n_iter = g * nch;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&sh.kv_full, 1);
+    for (int s = 0; s < ST; ++s) {
+      mbar_init(&sh.qd_full[s], 1);
+      mbar_init(&sh.qd_empty[s], 1);
+    }
+    mbar_init(&sh.sdp_full, 1);
+    mbar_init(&sh.st_free, 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sh.pds_full[s], 128);
+      mbar_init(&sh.mma_done[s], 1);
+      mbar_init(&sh.dq_free[s], 128);
+    }
+    sh.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sh.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sh.tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one() && n_iter > 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      prefetch_tmap(&tdo);
+      mbar_expect_tx(&sh.kv_full, 2 * kTileK);
+      for (int c = 0; c < D / 64; ++c) {
+        tma_load_3d(k_s + c * BN * 128, &tk, &sh.kv_full, c * 64, kvh, k0 + key0);
+        tma_load_3d(v_s + c * BN * 128, &tv, &sh.kv_full, c * 64, kvh, k0 + key0);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_iter; ++it) {
+        const int st = it % ST;
+        const int h = kvh * g + it / nch;
+        const int row = q0 + (c_lo + it % nch) * BQ;
+        if (!wait_bar(sh, &sh.qd_empty[st], ((it / ST) & 1) ^ 1, f.err)) break;
+        mbar_expect_tx(&sh.qd_full[st], 2 * kChunk);
+        uint8_t *dst = qd_s + st * 2 * kChunk;
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(dst + c * BQ * 128, &tq, &sh.qd_full[st], c * 64, h, row);
+          tma_load_3d(dst + kChunk + c * BQ * 128, &tdo, &sh.qd_full[st], c * 64, h, row);
+        }
+        issued = it + 1;
+      }
+      if (*(volatile int *)&sh.abort) {
+        int *noerr = nullptr;
+        mbar_wait(&sh.kv_full, 0, noerr);
+        for (int it = max(0, issued - ST); it < issued; ++it)
+          mbar_wait(&sh.qd_full[it % ST], (it / ST) & 1, noerr);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one() && n_iter > 0) {
+      constexpr int ab = IsBf16<T>::v;
+      constexpr uint32_t id_s = idesc_f16(128, BQ, ab, 0, 0);   // S^T, dP^T
+      constexpr uint32_t id_kv = idesc_f16(128, D, ab, 0, 1);   // dV, dK (B = dO/Q, MN-major)
+      constexpr uint32_t id_q = idesc_f16(128, BQ, ab, 1, 1);   // dQ^T (A = K^T, B = dS^T)
+      const uint32_t k_addr = smem_u32(k_s), v_addr = smem_u32(v_s);
+      const uint32_t qd_addr = smem_u32(qd_s), pt_addr = smem_u32(pt_s);
+      auto issue_sdp = [&](int it) -> bool {
+        const int st = it % ST;
+        if (!wait_bar(sh, &sh.qd_full[st], (it / ST) & 1, f.err)) return false;
+        tc_fence_after();
+        const uint32_t q_a = qd_addr + st * 2 * kChunk, do_a = q_a + kChunk;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+          const uint32_t qo = (kk / 4) * (BQ * 128) + (kk % 4) * 32;
+          mma_ss(tmem + kColS, smem_desc(k_addr + ko, 16, 1024), smem_desc(q_a + qo, 16, 1024),
+                 id_s, kk > 0);
+          mma_ss(tmem + kColDP, smem_desc(v_addr + ko, 16, 1024),
+                 smem_desc(do_a + qo, 16, 1024), id_s, kk > 0);
+        }
+        mma_commit(&sh.sdp_full);
+        return true;
+      };
+      bool ok = wait_bar(sh, &sh.kv_full, 0, f.err) && issue_sdp(0);
+      for (int it = 0; ok && it < n_iter; ++it) {
+        if (it + 1 < n_iter) {
+          if (!wait_bar(sh, &sh.st_free, it & 1, f.err)) break;
+          if (!issue_sdp(it + 1)) break;
+        }
+        const int buf = it & 1, st = it % ST;
+        if (!wait_bar(sh, &sh.pds_full[buf], (it >> 1) & 1, f.err)) break;
+        tc_fence_after();
+        const uint32_t q_a = qd_addr + st * 2 * kChunk, do_a = q_a + kChunk;
+        const uint32_t p_a = pt_addr + buf * 2 * kPT, ds_a = p_a + kPT;
+#pragma unroll
+        for (int kk = 0; kk < BQ / 16; ++kk) {
+          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+          mma_ss(tmem + kColDV, smem_desc(p_a + kk * 32, 16, 1024),
+                 smem_desc(do_a + kk * 16 * 128, BQ * 128, 1024), id_kv, acc);
+          mma_ss(tmem + kColDK, smem_desc(ds_a + kk * 32, 16, 1024),
+                 smem_desc(q_a + kk * 16 * 128, BQ * 128, 1024), id_kv, acc);
+        }
+        if (it >= 2 && !wait_bar(sh, &sh.dq_free[buf], ((it >> 1) - 1) & 1, f.err)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk)
+          mma_ss(tmem + kColDQ + buf * BQ, smem_desc(k_addr + kk * 16 * 128, BN * 128, 1024),
+                 smem_desc(ds_a + kk * 16 * 128, BQ * 128, 1024), id_q, kk > 0);
+        mma_commit(&sh.mma_done[buf]);
+        mma_commit(&sh.qd_empty[st]);
+      }
+    }
+  } else if (warp < 6) {
+    // ------------------------------------------------------------ P^T, dS^T
+    const int tid = threadIdx.x - 64;
+    const int j = 32 * (warp & 3) + lane;  // TMEM lane = key row of the block
+    const int kj = key0 + j;
+    const uint32_t row_t = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    int qlo, qhi;
+    query_range(kj, lq, lk, f.win_l, f.win_r, qlo, qhi);
+    if (kj >= lk) qhi = -1;
+    const bool cap = f.softcap > 0.f;
+    const float sl2 = f.scale * kLog2e, cap_in = cap ? f.scale / f.softcap : 0.f;
+    bool ok = true;
+    for (int it = 0; it < n_iter; ++it) {
+      const int buf = it & 1;
+      const int h = kvh * g + it / nch;
+      const int i0 = (c_lo + it % nch) * BQ;
+      {
+        const int e = tid & (BQ - 1), i = i0 + e;
+        if (tid < BQ)
+          sh.lse2[buf][e] = i < lq ? f.lse[f.seqs.lse_index(b, h, q0, i)] * kLog2e : 0.f;
+        else
+          sh.dsum[buf][e] = i < lq ? a.dsum[f.seqs.lse_index(b, h, q0, i)] : 0.f;
+      }
+      named_bar_sync(1, 128);
+      if (!wait_bar(sh, &sh.sdp_full, it & 1, f.err)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t su[BQ], du[BQ];
+      tmem_ld32(row_t + kColS, *reinterpret_cast<uint32_t(*)[32]>(su));
+      tmem_ld32(row_t + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
+      tmem_ld32(row_t + kColDP, *reinterpret_cast<uint32_t(*)[32]>(du));
+      tmem_ld32(row_t + kColDP + 32, *reinterpret_cast<uint32_t(*)[32]>(du + 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&sh.st_free);
+      uint32_t pk[BQ / 2], dk[BQ / 2];
+#pragma unroll
+      for (int e = 0; e < BQ; e += 2) {
+        float pv[2], dv[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int i = i0 + e + u;
+          const float s = __uint_as_float(su[e + u]);
+          float x, dcap = 1.f;
+          if (cap) {
+            const float t = tanhf(s * cap_in);
+            x = f.softcap * t * kLog2e;
+            dcap = 1.f - t * t;
+          } else {
+            x = s * sl2;
+          }
+          const bool vis = i >= qlo && i <= qhi;
+          const float p = vis ? ex2(x - sh.lse2[buf][e + u]) : 0.f;
+          pv[u] = p;
+          dv[u] = p * (__uint_as_float(du[e + u]) - sh.dsum[buf][e + u]) * dcap;
+        }
+        pk[e / 2] = Elem<T>::from_f2(pv[0], pv[1]);
+        dk[e / 2] = Elem<T>::from_f2(dv[0], dv[1]);
+      }
+      if (it >= 2 && !wait_bar(sh, &sh.mma_done[buf], ((it >> 1) - 1) & 1, f.err)) {
+        ok = false;
+        break;
+      }
+      uint8_t *p_s = pt_s + buf * 2 * kPT, *ds_s = p_s + kPT;
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc) {
+        const uint32_t off = j * 128 + ((cc ^ (j & 7)) << 4);
+        *reinterpret_cast<uint4 *>(p_s + off) =
+            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        *reinterpret_cast<uint4 *>(ds_s + off) =
+            make_uint4(dk[4 * cc], dk[4 * cc + 1], dk[4 * cc + 2], dk[4 * cc + 3]);
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      mbar_arrive(&sh.pds_full[buf]);
+    }
+    // dK, dV out of TMEM
+    if (ok && n_iter > 0) ok = wait_bar(sh, &sh.mma_done[(n_iter - 1) & 1], ((n_iter - 1) >> 1) & 1, f.err);
+    tc_fence_after();
+    if (ok && kj < lk) {
+      const int64_t off = ((int64_t)(k0 + kj) * f.hkv + kvh) * D;
+      T *dvr = static_cast<T *>(a.dv) + off;
+      T *dkr = static_cast<T *>(a.dk) + off;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          uint32_t u[32];
+          if (n_iter > 0) {
+            tmem_ld32(row_t + (which ? kColDK : kColDV) + c * 32, u);
+            tmem_wait_ld();
+          } else {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = 0u;
+          }
+          const float sc = which ? f.scale : 1.f;
+          uint32_t w[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            w[e] = Elem<T>::from_f2(__uint_as_float(u[2 * e]) * sc, __uint_as_float(u[2 * e + 1]) * sc);
+          uint4 *dst = reinterpret_cast<uint4 *>((which ? dkr : dvr) + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ
+    const int tid = threadIdx.x - 192;
+    const int dl = 32 * (warp & 3) + lane;  // TMEM lane = head-dim column
+    const uint32_t row_t = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    for (int it = 0; it < n_iter; ++it) {
+      const int buf = it & 1;
+      const int h = kvh * g + it / nch;
+      const int c = c_lo + it % nch;
+      const int i0 = c * BQ;
+      if (!wait_bar(sh, &sh.mma_done[buf], (it >> 1) & 1, f.err)) break;
+      tc_fence_after();
+      uint32_t u[BQ];
+      tmem_ld32(row_t + kColDQ + buf * BQ, *reinterpret_cast<uint32_t(*)[32]>(u));
+      tmem_ld32(row_t + kColDQ + buf * BQ + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive(&sh.dq_free[buf]);
+      int *turn_ctr = nullptr;
+      if (a.deterministic) {
+        // key blocks below this one that also add into chunk c go first
+        turn_ctr = sem + (int64_t)h * sem_per_head + (q0 / BQ + b) + c;
+        if (tid == 0) {
+          int turn = 0;
+          for (int nb2 = 0; nb2 < nb; ++nb2) {
+            int cl, nc;
+            chunk_range(nb2, lq, lk, f.win_l, f.win_r, cl, nc);
+            turn += (c >= cl && c < cl + nc) ? 1 : 0;
+          }
+          const uint64_t t0 = globaltimer();
+          int seen;
+          for (uint32_t spin = 0;; ++spin) {
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(turn_ctr) : "memory");
+            if (seen >= turn) break;
+            if ((spin & 63) == 63 && (globaltimer() - t0 > kWaitLimitNs || *(volatile int *)&sh.abort)) {
+              raise_error(f.err, kErrTimeout);
+              *(volatile int *)&sh.abort = 1;
+              break;
+            }
+          }
+        }
+        named_bar_sync(2, 128);
+      }
+      float *acc = a.dq_acc + ((int64_t)(q0 + i0) * f.hq + h) * D + dl;
+      const int rows = min(BQ, lq - i0);
+#pragma unroll
+      for (int e = 0; e < BQ; ++e)
+        if (e < rows) atomicAdd(acc + (int64_t)e * f.hq * D, __uint_as_float(u[e]));
+      if (a.deterministic) {
+        __threadfence();
+        named_bar_sync(2, 128);
+        if (tid == 0) atomicAdd(turn_ctr, 1);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// D_i = rowsum(dO_i * O_i) (fp32, LSE layout); zero the dQ accumulator and
+// the turn counters.  One warp per (row, head).
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int *sem, int64_t sem_count,
+                                                       int64_t rows) {
+  const FwdArgs &f = a.f;
+  const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+  for (int64_t x = w; x < rows * f.hq; x += nw) {
+    const int64_t row = x / f.hq;
+    const int h = (int)(x % f.hq);
+    const int64_t off = x * D + lane * 4;
+    float o[4], g[4];
+    load_vec<T, 4>(static_cast<const T *>(f.o) + off, o);
+    load_vec<T, 4>(static_cast<const T *>(a.dout) + off, g);
+    float s = o[0] * g[0] + o[1] * g[1] + o[2] * g[2] + o[3] * g[3];
+    s = warp_sum(s);
+    reinterpret_cast<float4 *>(a.dq_acc + off)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane == 0) {
+      int64_t li;
+      if (f.seqs.cu_q) {
+        li = (int64_t)h * f.seqs.total_q + row;
+      } else {
+        const int64_t bb = row / f.seqs.sq, i = row % f.seqs.sq;
+        li = (bb * f.hq + h) * f.seqs.sq + i;
+      }
+      a.dsum[li] = s;
+    }
+  }
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (int64_t x = t; x < sem_count; x += (int64_t)gridDim.x * blockDim.x) sem[x] = 0;
+}
+
+// dQ = scale * dQ_acc -> dtype.
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdArgs a, int64_t n4) {
+  for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n4;
+       x += (int64_t)gridDim.x * blockDim.x) {
+    const float4 v = reinterpret_cast<const float4 *>(a.dq_acc)[x];
+    const float s = a.f.scale;
+    uint2 out{Elem<T>::from_f2(v.x * s, v.y * s), Elem<T>::from_f2(v.z * s, v.w * s)};
+    reinterpret_cast<uint2 *>(a.dq)[x] = out;
+  }
+}
+
+template <typename T>
+cudaError_t bwd_tc(const BwdArgs &a, int *sem, int sem_per_head, int sms, cudaStream_t st) {
+  const FwdArgs &f = a.f;
+  const int64_t rows_q = f.seqs.cu_q ? f.seqs.total_q : (int64_t)f.batch * f.seqs.sq;
+  const int64_t rows_k = f.seqs.cu_k ? f.seqs.total_k : (int64_t)f.batch * f.seqs.sk;
+  const int64_t sem_count = (int64_t)sem_per_head * f.hq;
+  const int prep_blocks = (int)std::min<int64_t>((rows_q * f.hq + 7) / 8, (int64_t)sms * 16);
+  if (rows_q > 0) {
+    bwd_prep_kernel<T><<<std::max(prep_blocks, 1), 256, 0, st>>>(a, sem, sem_count, rows_q);
+    count_launches(1);
+  }
+  if (rows_k > 0 && rows_q > 0) {
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_map_3d(&tq, f.q, f.dtype, rows_q, f.hq, D, BQ) ||
+        !make_map_3d(&tdo, a.dout, f.dtype, rows_q, f.hq, D, BQ) ||
+        !make_map_3d(&tk, f.k, f.dtype, rows_k, f.hkv, D, BN) ||
+        !make_map_3d(&tv, f.v, f.dtype, rows_k, f.hkv, D, BN))
+      return cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    const int n_blocks = (f.seqs.sk + BN - 1) / BN;
+    const int64_t grid = (int64_t)n_blocks * f.hkv * f.batch;
+    if (grid > INT32_MAX) return cudaErrorInvalidValue;
+    bwd_tc_kernel<T><<<(unsigned)grid, kThreads, kSmem, st>>>(tq, tk, tv, tdo, a, n_blocks, sem,
+                                                              sem_per_head);
+    count_launches(1);
+  } else if (rows_k > 0) {  // no queries: the key gradients are zero
+    const size_t bytes = (size_t)rows_k * f.hkv * D * 2;
+    cudaError_t e = cudaMemsetAsync(a.dk, 0, bytes, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a.dv, 0, bytes, st);
+    if (e != cudaSuccess) return e;
+  }
+  if (rows_q > 0) {
+    const int64_t n4 = rows_q * f.hq * D / 4;
+    const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, (int64_t)sms * 16);
+    bwd_dq_convert_kernel<T><<<std::max(blocks, 1), 256, 0, st>>>(a, n4);
+    count_launches(1);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_tc(const BwdArgs &a, int *sem, int sem_per_head, int sms,
+                          cudaStream_t st) {
+  if (a.f.d != D) return cudaErrorInvalidValue;
+  return a.f.dtype == ATTN_BF16 ? bwd_tc<__nv_bfloat16>(a, sem, sem_per_head, sms, st)
+                                : bwd_tc<__half>(a, sem, sem_per_head, sms, st);
+}
+
+}  // namespace attn

@@ -26,6 +26,38 @@
 #include "sm103.cuh"
 
 namespace attn {
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+}  // namespace
+
+// (rows, heads, D) tensor, box {64, 1, box_rows}, 128-byte swizzle.
+bool make_map_3d(CUtensorMap *m, const void *base, int dtype, int64_t rows, int heads, int d,
+              int box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+             3, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 namespace {
 using namespace sm103;
 
@@ -347,34 +379,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ---------------------------------------------------------------- host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess)
-      p = nullptr;
-    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }();
-  return fn;
-}
-
-// (rows, heads, D) tensor, box {64, 1, box_rows}, 128-byte swizzle.
-bool make_map(CUtensorMap *m, const void *base, int dtype, int64_t rows, int heads, int d,
-              int box_rows) {
-  auto enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
-  cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-             3, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <typename T, int D, int BN>
 cudaError_t fwd_tc(const FwdArgs &a, cudaStream_t st) {
   using C = FwdCfg<D, BN>;
@@ -382,9 +386,9 @@ cudaError_t fwd_tc(const FwdArgs &a, cudaStream_t st) {
   const int64_t rows_k = a.seqs.cu_k ? a.seqs.total_k : (int64_t)a.batch * a.seqs.sk;
   if (rows_k == 0) return launch_fwd_simt(a, st);  // no keys: every row is empty
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, a.q, a.dtype, rows_q, a.hq, D, kBM) ||
-      !make_map(&tk, a.k, a.dtype, rows_k, a.hkv, D, BN) ||
-      !make_map(&tv, a.v, a.dtype, rows_k, a.hkv, D, BN))
+  if (!make_map_3d(&tq, a.q, a.dtype, rows_q, a.hq, D, kBM) ||
+      !make_map_3d(&tk, a.k, a.dtype, rows_k, a.hkv, D, BN) ||
+      !make_map_3d(&tv, a.v, a.dtype, rows_k, a.hkv, D, BN))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<T, D, BN>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
