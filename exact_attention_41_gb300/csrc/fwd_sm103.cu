@@ -62,25 +62,31 @@ namespace {
 using namespace sm103;
 
 constexpr int kBM = 128;
-constexpr int kThreads = 192;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when max grows > 256x
 
-template <int D, int BN>
+// NT query tiles of 128 rows per CTA.  NT = 2 (d <= 128): one softmax
+// warpgroup per tile, TMEM = [O_0 | O_1 | S_0 | S_1]; the MMA warp alternates
+// between the tiles so one tile's softmax overlaps the other tile's MMAs, and
+// every K/V tile staged in shared memory serves 256 query rows.  NT = 1
+// (d = 256): TMEM = [O | S_a | S_b], S double-buffered instead.
+template <int D, int BN, int NT>
 struct FwdCfg {
   static constexpr int kStages = (D == 64) ? 3 : 2;
-  static constexpr int kQBytes = kBM * D * 2;
+  static constexpr int kQBytes = kBM * D * 2;  // one tile
   static constexpr int kKVBytes = BN * D * 2;
-  static constexpr int kSmemData = kQBytes + 2 * kStages * kKVBytes;
+  static constexpr int kSmemData = NT * kQBytes + 2 * kStages * kKVBytes;
   // at least ~120 KB so that one CTA owns the SM (and all 512 TMEM columns)
   static constexpr int kSmem = (kSmemData + 1024 > 120 * 1024 ? kSmemData + 1024 : 120 * 1024);
-  static constexpr int kSCol0 = D;
+  static constexpr int kSCol0 = NT * D;
   static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kThreads = 64 + 128 * NT;
+  static_assert(NT * D + 2 * BN <= 512, "TMEM budget");
 };
 
 struct Shared {
   uint64_t q_full;
   uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
-  uint64_t s_full[2], p_full[2], o_done;
+  uint64_t s_full[2], p_full[2], o_done[2];
   uint32_t tmem_base;
   int abort;
 };
@@ -115,34 +121,34 @@ template <> struct IsBf16<__nv_bfloat16> { static constexpr int v = 1; };
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float a, float b) { return Elem<T>::from_f2(a, b); }
 
-template <typename T, int D, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+template <typename T, int D, int BN, int NT>
+__global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdArgs a, const int m_blocks) {
-  using C = FwdCfg<D, BN>;
+  using C = FwdCfg<D, BN, NT>;
   constexpr int ST = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   uint8_t *q_s = smem;
-  uint8_t *k_s = smem + C::kQBytes;
+  uint8_t *k_s = smem + NT * C::kQBytes;
   uint8_t *v_s = k_s + ST * C::kKVBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // CTA -> (query tile, batch, head): heaviest tiles first, heads fastest.
+  // CTA -> (query block, batch, head): heaviest blocks first, heads fastest.
   const int bid = blockIdx.x;
   const int h = bid % a.hq;
   const int b = (bid / a.hq) % a.batch;
   const int mb = m_blocks - 1 - bid / (a.hq * a.batch);
   int q0, lq, k0, lk;
   if (!a.seqs.get(b, q0, lq, k0, lk, a.err)) return;
-  const int m0 = mb * kBM;
+  const int m0 = mb * (kBM * NT);
   if (m0 >= lq) return;
   const int kvh = h / (a.hq / a.hkv);
-  const int m_last = min(m0 + kBM, lq) - 1;
+  const int m_last = min(m0 + kBM * NT, lq) - 1;
 
-  // key tiles any row of this query tile may see
+  // key tiles any row of this query block may see
   int lo_first, hi_first, lo_last, hi_last;
   key_range(m0, lq, lk, a.win_l, a.win_r, lo_first, hi_first);
   key_range(m_last, lq, lk, a.win_l, a.win_r, lo_last, hi_last);
@@ -163,8 +169,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sh.s_full[s], 1);
       mbar_init(&sh.p_full[s], kBM);
+      mbar_init(&sh.o_done[s], 1);
     }
-    mbar_init(&sh.o_done, 1);
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -183,9 +189,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
-      mbar_expect_tx(&sh.q_full, C::kQBytes);
-      for (int c = 0; c < D / 64; ++c)
-        tma_load_3d(q_s + c * kBM * 128, &tq, &sh.q_full, c * 64, h, q0 + m0);
+      mbar_expect_tx(&sh.q_full, NT * C::kQBytes);
+      for (int t = 0; t < NT; ++t)
+        for (int c = 0; c < D / 64; ++c)
+          tma_load_3d(q_s + t * C::kQBytes + c * kBM * 128, &tq, &sh.q_full, c * 64, h,
+                      q0 + m0 + t * kBM);
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
         const int st = j % ST;
@@ -220,50 +228,100 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_s = idesc_f16(kBM, BN, ab, 0, 0);
       constexpr uint32_t id_o = idesc_f16(kBM, D, ab, 0, 1);
       const uint32_t q_addr = smem_u32(q_s), k_addr = smem_u32(k_s), v_addr = smem_u32(v_s);
-      auto issue_s = [&](int j) -> bool {
+      // S_t = Q_t K_j^T into TMEM column `dcol`
+      auto mma_s = [&](int t, int j, uint32_t dcol) {
         const int st = j % ST;
-        if (!wait_bar(sh, &sh.k_full[st], (j / ST) & 1, a.err)) return false;
-        tc_fence_after();
-        const uint32_t dcol = tmem + C::kSCol0 + (j & 1) * BN;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = smem_desc(q_addr + (kk / 4) * (kBM * 128) + (kk % 4) * 32, 16, 1024);
+          const uint64_t ad = smem_desc(
+              q_addr + t * C::kQBytes + (kk / 4) * (kBM * 128) + (kk % 4) * 32, 16, 1024);
           const uint64_t bd = smem_desc(k_addr + st * C::kKVBytes + (kk / 4) * (BN * 128) +
                                             (kk % 4) * 32, 16, 1024);
           mma_ss(dcol, ad, bd, id_s, kk > 0);
         }
-        mma_commit(&sh.s_full[j & 1]);
-        mma_commit(&sh.k_empty[st]);
-        return true;
       };
-      bool ok = nt == 0 || (wait_bar(sh, &sh.q_full, 0, a.err) && issue_s(0));
-      for (int j = 0; ok && j < nt; ++j) {
-        if (j + 1 < nt && !issue_s(j + 1)) break;
-        if (!wait_bar(sh, &sh.p_full[j & 1], (j >> 1) & 1, a.err)) break;
+      // O_t += P V_j with P read from TMEM column `pcol`
+      auto mma_pv = [&](int t, int j, uint32_t pcol) {
         const int st = j % ST;
-        if (!wait_bar(sh, &sh.v_full[st], (j / ST) & 1, a.err)) break;
-        tc_fence_after();
-        const uint32_t pcol = tmem + C::kSCol0 + (j & 1) * BN;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t bd = smem_desc(v_addr + st * C::kKVBytes + kk * 16 * 128, BN * 128, 1024);
-          mma_ts(tmem, pcol + kk * 8, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + t * D, pcol + kk * 8, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(&sh.o_done);
-        mma_commit(&sh.v_empty[st]);
+      };
+      auto k_ready = [&](int j) {
+        const bool r = wait_bar(sh, &sh.k_full[j % ST], (j / ST) & 1, a.err);
+        tc_fence_after();
+        return r;
+      };
+      auto v_ready = [&](int j) {
+        const bool r = wait_bar(sh, &sh.v_full[j % ST], (j / ST) & 1, a.err);
+        tc_fence_after();
+        return r;
+      };
+      if (NT == 2) {
+        // S_0(0) S_1(0) | PV_0(j) S_0(j+1) PV_1(j) S_1(j+1) | ...
+        bool ok = nt == 0 || (wait_bar(sh, &sh.q_full, 0, a.err) && k_ready(0));
+        if (ok && nt > 0) {
+          for (int t = 0; t < NT; ++t) {
+            mma_s(t, 0, tmem + C::kSCol0 + t * BN);
+            mma_commit(&sh.s_full[t]);
+          }
+          mma_commit(&sh.k_empty[0]);
+        }
+        for (int j = 0; ok && j < nt; ++j) {
+          for (int t = 0; t < NT && ok; ++t) {
+            const uint32_t scol = tmem + C::kSCol0 + t * BN;
+            if (!wait_bar(sh, &sh.p_full[t], j & 1, a.err)) { ok = false; break; }
+            tc_fence_after();
+            if (t == 0 && !v_ready(j)) { ok = false; break; }
+            mma_pv(t, j, scol);
+            mma_commit(&sh.o_done[t]);
+            if (t == NT - 1) mma_commit(&sh.v_empty[j % ST]);
+            if (j + 1 < nt) {
+              if (t == 0 && !k_ready(j + 1)) { ok = false; break; }
+              mma_s(t, j + 1, scol);
+              mma_commit(&sh.s_full[t]);
+              if (t == NT - 1) mma_commit(&sh.k_empty[(j + 1) % ST]);
+            }
+          }
+        }
+      } else {
+        bool ok = nt == 0 || (wait_bar(sh, &sh.q_full, 0, a.err) && k_ready(0));
+        if (ok && nt > 0) {
+          mma_s(0, 0, tmem + C::kSCol0);
+          mma_commit(&sh.s_full[0]);
+          mma_commit(&sh.k_empty[0]);
+        }
+        for (int j = 0; ok && j < nt; ++j) {
+          if (j + 1 < nt) {
+            if (!k_ready(j + 1)) break;
+            mma_s(0, j + 1, tmem + C::kSCol0 + ((j + 1) & 1) * BN);
+            mma_commit(&sh.s_full[(j + 1) & 1]);
+            mma_commit(&sh.k_empty[(j + 1) % ST]);
+          }
+          if (!wait_bar(sh, &sh.p_full[j & 1], (j >> 1) & 1, a.err)) break;
+          tc_fence_after();
+          if (!v_ready(j)) break;
+          mma_pv(0, j, tmem + C::kSCol0 + (j & 1) * BN);
+          mma_commit(&sh.o_done[0]);
+          mma_commit(&sh.v_empty[j % ST]);
+        }
       }
     }
   } else {
     // ------------------------------------------------------------ softmax
+    const int t = (warp - 2) >> 2;         // query tile of this warpgroup
     const int r = 32 * (warp & 3) + lane;  // TMEM lane = query row in the tile
-    const int i = m0 + r;
-    const uint32_t row_t = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    const int i = m0 + t * kBM + r;
+    const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+    const uint32_t o_t = tmem + lane_off + t * D;
     int lo_i, hi_i;
     key_range(i, lq, lk, a.win_l, a.win_r, lo_i, hi_i);
     // tiles that need no mask: every row of the tile sees every key in them
     int lo_tile_max, hi_tile_min, dummy;
-    key_range(m0 + kBM - 1, lq, lk, a.win_l, a.win_r, lo_tile_max, dummy);
-    key_range(m0, lq, lk, a.win_l, a.win_r, dummy, hi_tile_min);
+    key_range(m0 + t * kBM + kBM - 1, lq, lk, a.win_l, a.win_r, lo_tile_max, dummy);
+    key_range(m0 + t * kBM, lq, lk, a.win_l, a.win_r, dummy, hi_tile_min);
     const float sl2 = a.scale * kLog2e;
     const bool cap = a.softcap > 0.f;
     const float cap_in = cap ? a.scale / a.softcap : 0.f, cap_out = a.softcap * kLog2e;
@@ -271,31 +329,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
       const int key0 = (n_lo + j) * BN;
-      if (!wait_bar(sh, &sh.s_full[j & 1], (j >> 1) & 1, a.err)) { ok = false; break; }
+      const int sb = NT == 2 ? t : (j & 1);                 // S/P buffer and its barriers
+      const uint32_t s_par = NT == 2 ? (j & 1) : ((j >> 1) & 1);
+      if (!wait_bar(sh, &sh.s_full[sb], s_par, a.err)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t scol = row_t + C::kSCol0 + (j & 1) * BN;
+      const uint32_t scol = tmem + lane_off + C::kSCol0 + sb * BN;
       float x[BN];
+      {
+        uint32_t u[BN];
 #pragma unroll
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t u[32];
-        tmem_ld32(scol + c * 32, u);
+        for (int c = 0; c < BN / 32; ++c)
+          tmem_ld32(scol + c * 32, *reinterpret_cast<uint32_t(*)[32]>(u + c * 32));
         tmem_wait_ld();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(u[e]);
+        for (int e = 0; e < BN; ++e) x[e] = __uint_as_float(u[e]);
       }
       const bool need_mask = key0 < lo_tile_max || key0 + BN - 1 > hi_tile_min;
+      if (need_mask) {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) {
+          const int kj = key0 + e;
+          if (kj < lo_i || kj > hi_i) x[e] = -INFINITY;
+        }
+      }
+      if (cap) {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) x[e] = cap_out * tanhf(x[e] * cap_in);
+      }
+      // raw-score max: scale and softcap preserve the order (scale >= 0)
       float mt = -INFINITY;
 #pragma unroll
-      for (int e = 0; e < BN; ++e) {
-        float v = cap ? cap_out * tanhf(x[e] * cap_in) : x[e] * sl2;
-        if (need_mask) {
-          const int kj = key0 + e;
-          if (kj < lo_i || kj > hi_i) v = -INFINITY;
-        }
-        x[e] = v;
-        mt = fmaxf(mt, v);
-      }
-      const float m_new = fmaxf(m_ref, mt);
+      for (int e = 0; e < BN; ++e) mt = fmaxf(mt, x[e]);
+      const float f = cap ? 1.f : sl2;  // x * f is the score in log2 units
+      const float m_new = fmaxf(m_ref, mt * f);
       const bool rescale = m_new > m_ref + kRescaleThreshold;
       float alpha = 1.f;
       if (rescale) {
@@ -303,44 +369,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= alpha;
         m_ref = m_new;
       }
-      const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-      float rs = 0.f;
+      const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+      float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(x[c * 32 + 2 * e] - m_use);
-          const float p1 = ex2(x[c * 32 + 2 * e + 1] - m_use);
-          rs += p0 + p1;
+          const float p0 = ex2(fmaf(x[c * 32 + 2 * e], f, neg_m));
+          const float p1 = ex2(fmaf(x[c * 32 + 2 * e + 1], f, neg_m));
+          rs0 += p0;
+          rs1 += p1;
           pk[e] = pack2<T>(p0, p1);
         }
         tmem_st16(scol + c * 16, pk);
       }
-      l += rs;
+      l += rs0 + rs1;
       tmem_wait_st();
       if (j > 0) {
         // O holds P_{j-1} V_{j-1} once this completes; only then may it be rescaled
-        if (!wait_bar(sh, &sh.o_done, (j - 1) & 1, a.err)) { ok = false; break; }
+        if (!wait_bar(sh, &sh.o_done[t], (j - 1) & 1, a.err)) { ok = false; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t u[32];
-            tmem_ld32(row_t + c * 32, u);
+            tmem_ld32(o_t + c * 32, u);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * alpha);
-            tmem_st32(row_t + c * 32, u);
+            tmem_st32(o_t + c * 32, u);
           }
           tmem_wait_st();
         }
       }
       tc_fence_before();
-      mbar_arrive(&sh.p_full[j & 1]);
+      mbar_arrive(&sh.p_full[sb]);
     }
     // epilogue: O / l -> dtype, LSE = ln(sum exp(s))
-    if (ok && nt > 0) ok = wait_bar(sh, &sh.o_done, (nt - 1) & 1, a.err);
+    if (ok && nt > 0) ok = wait_bar(sh, &sh.o_done[t], (nt - 1) & 1, a.err);
     tc_fence_after();
     if (ok) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -350,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < D / 32; ++c) {
         uint32_t u[32];
         if (nt > 0) {
-          tmem_ld32(row_t + c * 32, u);
+          tmem_ld32(o_t + c * 32, u);
           tmem_wait_ld();
         } else {
 #pragma unroll
@@ -377,11 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-// ---------------------------------------------------------------- host side
-
-template <typename T, int D, int BN>
+template <typename T, int D, int BN, int NT>
 cudaError_t fwd_tc(const FwdArgs &a, cudaStream_t st) {
-  using C = FwdCfg<D, BN>;
+  using C = FwdCfg<D, BN, NT>;
   const int64_t rows_q = a.seqs.cu_q ? a.seqs.total_q : (int64_t)a.batch * a.seqs.sq;
   const int64_t rows_k = a.seqs.cu_k ? a.seqs.total_k : (int64_t)a.batch * a.seqs.sk;
   if (rows_k == 0) return launch_fwd_simt(a, st);  // no keys: every row is empty
@@ -390,14 +455,15 @@ cudaError_t fwd_tc(const FwdArgs &a, cudaStream_t st) {
       !make_map_3d(&tk, a.k, a.dtype, rows_k, a.hkv, D, BN) ||
       !make_map_3d(&tv, a.v, a.dtype, rows_k, a.hkv, D, BN))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<T, D, BN>,
+  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<T, D, BN, NT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  const int m_blocks = (a.seqs.sq + kBM - 1) / kBM;
+  const int m_blocks = (a.seqs.sq + kBM * NT - 1) / (kBM * NT);
   const int64_t grid = (int64_t)m_blocks * a.hq * a.batch;
   if (grid == 0) return cudaSuccess;
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
-  fwd_tc_kernel<T, D, BN><<<(unsigned)grid, kThreads, C::kSmem, st>>>(tq, tk, tv, a, m_blocks);
+  fwd_tc_kernel<T, D, BN, NT><<<(unsigned)grid, C::kThreads, C::kSmem, st>>>(tq, tk, tv, a,
+                                                                          m_blocks);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -407,9 +473,9 @@ cudaError_t fwd_tc(const FwdArgs &a, cudaStream_t st) {
 cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t st) {
   const bool bf = a.dtype == ATTN_BF16;
   switch (a.d) {
-    case 64: return bf ? fwd_tc<__nv_bfloat16, 64, 128>(a, st) : fwd_tc<__half, 64, 128>(a, st);
-    case 128: return bf ? fwd_tc<__nv_bfloat16, 128, 128>(a, st) : fwd_tc<__half, 128, 128>(a, st);
-    case 256: return bf ? fwd_tc<__nv_bfloat16, 256, 64>(a, st) : fwd_tc<__half, 256, 64>(a, st);
+    case 64: return bf ? fwd_tc<__nv_bfloat16, 64, 128, 2>(a, st) : fwd_tc<__half, 64, 128, 2>(a, st);
+    case 128: return bf ? fwd_tc<__nv_bfloat16, 128, 128, 2>(a, st) : fwd_tc<__half, 128, 128, 2>(a, st);
+    case 256: return bf ? fwd_tc<__nv_bfloat16, 256, 64, 1>(a, st) : fwd_tc<__half, 256, 64, 1>(a, st);
   }
   return cudaErrorInvalidValue;
 }
