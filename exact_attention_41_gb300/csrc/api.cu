@@ -51,7 +51,7 @@ attn_status check_common(int dtype, int hq, int hkv, int d, float scale, int win
   if (dtype != ATTN_F16 && dtype != ATTN_BF16) return ATTN_ERR_INVALID;
   if (hq <= 0 || hkv <= 0 || hq % hkv != 0) return ATTN_ERR_INVALID;
   if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
-  if (!isfinite(scale)) return ATTN_ERR_INVALID;
+  if (!isfinite(scale) || scale < 0.f) return ATTN_ERR_INVALID;
   if (isnan(softcap)) return ATTN_ERR_INVALID;
   if (win_l < -1 || win_r < -1) return ATTN_ERR_INVALID;
   if (causal) win_r = 0;

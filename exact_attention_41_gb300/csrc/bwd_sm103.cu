@@ -36,9 +36,6 @@
 
 namespace attn {
 
-bool make_map_3d(CUtensorMap *m, const void *base, int dtype, int64_t rows, int heads, int d,
-                 int box_rows);
-
 namespace {
 using namespace sm103;
 

@@ -168,9 +168,19 @@ cudaError_t decode(const DecodeArgs &a, cudaStream_t st) {
   if (a.s_new > 0) {
     append_kernel<T><<<dim3(a.s_new, a.b), 128, 0, st>>>(a);
   }
-  decode_rows_kernel<T, D><<<dim3(a.num_splits, a.hq, a.b), kWarps * 32, 0, st>>>(a);
-  if (a.num_splits > 1) combine_kernel<T, D><<<dim3(a.sq, a.hq, a.b), 32, 0, st>>>(a);
-  count_launches((a.s_new > 0) + 1 + (a.num_splits > 1));
+  count_launches(a.s_new > 0);
+  // tensor-core kernel (d = 128, g * sq <= 32); warp-per-row kernel otherwise
+  cudaError_t e = launch_decode_tc(a, st);
+  if (e == cudaErrorNotSupported) {
+    decode_rows_kernel<T, D><<<dim3(a.num_splits, a.hq, a.b), kWarps * 32, 0, st>>>(a);
+    count_launches(1);
+  } else if (e != cudaSuccess) {
+    return e;
+  }
+  if (a.num_splits > 1) {
+    combine_kernel<T, D><<<dim3(a.sq, a.hq, a.b), 32, 0, st>>>(a);
+    count_launches(1);
+  }
   return cudaGetLastError();
 }
 

@@ -1,6 +1,8 @@
 // Internal launcher interface between the C ABI (api.cu) and the kernels.
 #pragma once
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 
 namespace attn {
@@ -42,6 +44,14 @@ struct DecodeArgs {
   float *lse_part;              // (splits, b, hq, sq)
   int *err;
 };
+
+// cuTensorMapEncodeTiled from the driver (looked up once), or nullptr.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+// 3-D (rows, heads, d) tensor map, box {64, 1, box_rows}, 128-byte swizzle.
+bool make_map_3d(CUtensorMap *m, const void *base, int dtype, int64_t rows, int heads, int d,
+                 int box_rows);
+// Tensor-core decode; cudaErrorNotSupported for shapes it does not handle.
+cudaError_t launch_decode_tc(const DecodeArgs &a, cudaStream_t st);
 
 // Adds n to the library's launch counter (attn_launch_count).
 void count_launches(int n);

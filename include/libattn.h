@@ -15,6 +15,9 @@
  *   P = softmax over the visible keys, O = P V,  LSE_i = m_i + ln(l_i)
  *          (the saved softmax statistics of "FlashAttention完整说明" §二.2)
  *
+ * scale must be finite and >= 0 (the FlashAttention default is 1/sqrt(d),
+ * Inference Cookbook FAQ Q12); softcap <= 0 turns the cap off.
+ *
  * Rows with no visible key produce O = 0 and LSE = -inf and get zero
  * gradient.  The score matrix is never written to memory: the kernels tile
  * Q/K/V through shared memory and use an online softmax (§二.1), and the

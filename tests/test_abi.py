@@ -54,6 +54,7 @@ def fwd(lib, **over):
 @pytest.mark.parametrize("over,status", [
     (dict(d=96), 2), (dict(d=32), 2), (dict(hq=6, hkv=4), 1), (dict(hkv=0), 1),
     (dict(dtype=7), 1), (dict(wl=-2), 1), (dict(wr=-5), 1), (dict(scale=float("inf")), 1),
+    (dict(scale=-0.5), 1), (dict(scale=float("nan")), 1),
     (dict(cap=float("nan")), 1), (dict(b=-1), 1), (dict(sq=-3), 1),
 ])
 def test_invalid_arguments_are_rejected_on_host(lib, over, status):
