@@ -56,6 +56,7 @@ struct Shared {
   uint64_t qd_full[ST], qd_empty[ST];
   uint64_t sdp_full, st_free;
   uint64_t pds_full[2], mma_done[2], dq_free[2];
+  uint64_t grp_p, grp_q;  // bounded barriers of the P^T warpgroup and the dQ warpgroup
   uint32_t tmem_base;
   int abort;
   float lse2[2][BQ];
@@ -83,6 +84,12 @@ __device__ __forceinline__ bool wait_bar(Shared &sh, uint64_t *bar, uint32_t par
       }
     }
   }
+}
+
+// The same wait taken by a whole warp with one answer, so warp-collective
+// tcgen05 loads/stores that follow are never reached by part of a warp.
+__device__ __forceinline__ bool wait_warp(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
+  return __all_sync(0xffffffffu, wait_bar(sh, bar, parity, err));
 }
 
 template <typename T> struct IsBf16 { static constexpr int v = 0; };
@@ -153,6 +160,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.mma_done[s], 1);
       mbar_init(&sh.dq_free[s], 128);
     }
+    mbar_init(&sh.grp_p, 128);
+    mbar_init(&sh.grp_q, 128);
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -276,8 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
           sh.dsum[buf][e] = i < lq ? a.dsum[f.seqs.lse_index(b, h, q0, i)] : 0.f;
       }
-      named_bar_sync(1, 128);
-      if (!wait_bar(sh, &sh.sdp_full, it & 1, f.err)) { ok = false; break; }
+      mbar_arrive(&sh.grp_p);  // the chunk's LSE and D are in shared memory
+      if (!wait_warp(sh, &sh.grp_p, it & 1, f.err)) { ok = false; break; }
+      if (!wait_warp(sh, &sh.sdp_full, it & 1, f.err)) { ok = false; break; }
       tc_fence_after();
       uint32_t su[BQ], du[BQ];
       tmem_ld32(row_t + kColS, *reinterpret_cast<uint32_t(*)[32]>(su));
@@ -311,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pk[e / 2] = Elem<T>::from_f2(pv[0], pv[1]);
         dk[e / 2] = Elem<T>::from_f2(dv[0], dv[1]);
       }
-      if (it >= 2 && !wait_bar(sh, &sh.mma_done[buf], ((it >> 1) - 1) & 1, f.err)) {
+      if (it >= 2 && !wait_warp(sh, &sh.mma_done[buf], ((it >> 1) - 1) & 1, f.err)) {
         ok = false;
         break;
       }
@@ -328,9 +338,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(&sh.pds_full[buf]);
     }
     // dK, dV out of TMEM
-    if (ok && n_iter > 0) ok = wait_bar(sh, &sh.mma_done[(n_iter - 1) & 1], ((n_iter - 1) >> 1) & 1, f.err);
+    if (ok && n_iter > 0)
+      ok = wait_warp(sh, &sh.mma_done[(n_iter - 1) & 1], ((n_iter - 1) >> 1) & 1, f.err);
+    ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
-    if (ok && kj < lk) {
+    // tcgen05.ld is warp-collective: every lane loads, only real keys store
+    if (ok) {
       const int64_t off = ((int64_t)(k0 + kj) * f.hkv + kvh) * D;
       T *dvr = static_cast<T *>(a.dv) + off;
       T *dkr = static_cast<T *>(a.dk) + off;
@@ -351,9 +364,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             w[e] = Elem<T>::from_f2(__uint_as_float(u[2 * e]) * sc, __uint_as_float(u[2 * e + 1]) * sc);
-          uint4 *dst = reinterpret_cast<uint4 *>((which ? dkr : dvr) + c * 32);
+          if (kj < lk) {
+            uint4 *dst = reinterpret_cast<uint4 *>((which ? dkr : dvr) + c * 32);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            for (int e = 0; e < 4; ++e)
+              dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          }
         }
       }
     }
@@ -367,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int h = kvh * g + it / nch;
       const int c = c_lo + it % nch;
       const int i0 = c * BQ;
-      if (!wait_bar(sh, &sh.mma_done[buf], (it >> 1) & 1, f.err)) break;
+      if (!wait_warp(sh, &sh.mma_done[buf], (it >> 1) & 1, f.err)) break;
       tc_fence_after();
       uint32_t u[BQ];
       tmem_ld32(row_t + kColDQ + buf * BQ, *reinterpret_cast<uint32_t(*)[32]>(u));
@@ -398,7 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        named_bar_sync(2, 128);
+        mbar_arrive(&sh.grp_q);  // thread 0 has seen this key block's turn
+        if (!wait_warp(sh, &sh.grp_q, 0, f.err)) break;
       }
       float *acc = a.dq_acc + ((int64_t)(q0 + i0) * f.hq + h) * D + dl;
       const int rows = min(BQ, lq - i0);
@@ -407,7 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (e < rows) atomicAdd(acc + (int64_t)e * f.hq * D, __uint_as_float(u[e]));
       if (a.deterministic) {
         __threadfence();
-        named_bar_sync(2, 128);
+        mbar_arrive(&sh.grp_q);  // every add of this key block is performed
+        if (!wait_warp(sh, &sh.grp_q, 1, f.err)) break;
         if (tid == 0) atomicAdd(turn_ctr, 1);
       }
     }

@@ -84,6 +84,12 @@ __device__ __forceinline__ bool wait_bar(DecShared &sh, uint64_t *bar, uint32_t 
   }
 }
 
+// The same wait taken by a whole warp with one answer, so warp-collective
+// tcgen05 loads/stores that follow are never reached by part of a warp.
+__device__ __forceinline__ bool wait_warp(DecShared &sh, uint64_t *bar, uint32_t parity, int *err) {
+  return __all_sync(0xffffffffu, wait_bar(sh, bar, parity, err));
+}
+
 template <typename T> struct IsBf16 { static constexpr int v = 0; };
 template <> struct IsBf16<__nv_bfloat16> { static constexpr int v = 1; };
 
@@ -293,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const int key = (t_first + j) * BK + jl;
-      if (!wait_bar(sh, &sh.s_full[j & 1], (j >> 1) & 1, a.err)) { ok = false; break; }
+      if (!wait_warp(sh, &sh.s_full[j & 1], (j >> 1) & 1, a.err)) { ok = false; break; }
       tc_fence_after();
       uint32_t su[RP];
       tmem_ld_rp<RP>(tmem + lane_off + C::kColS + (j & 1) * RP, su);
@@ -322,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float(*wm)[32] = sh.wmax[j & 1];
       if (lane < RP) wm[w4][lane] = mine;
       mbar_arrive(&sh.grp);
-      if (!wait_bar(sh, &sh.grp, j & 1, a.err)) { ok = false; break; }
+      if (!wait_warp(sh, &sh.grp, j & 1, a.err)) { ok = false; break; }
       float alpha[RP];
       bool any_rescale = false;
 #pragma unroll
@@ -347,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // PV(j-1) must be done before its P buffer's twin is rewritten and O^T rescaled
       if (j > 0) {
-        if (!wait_bar(sh, &sh.o_done, (j - 1) & 1, a.err)) { ok = false; break; }
+        if (!wait_warp(sh, &sh.o_done, (j - 1) & 1, a.err)) { ok = false; break; }
         tc_fence_after();
       }
       uint8_t *pb = p_s + (j & 1) * C::kPBytes + (jl / 64) * (RP * 128);
@@ -365,23 +371,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st_rp<RP>(tmem + lane_off + C::kColO, ou);
         tmem_wait_st();
       }
-      if (key >= L) {
+      if (__any_sync(0xffffffffu, key >= L)) {
         // keys past the cache end: their V rows may hold anything, and 0 * NaN
         // would poison O^T, so zero them (the TMA load must have landed)
-        if (!wait_bar(sh, &sh.v_full[j % ST], (j / ST) & 1, a.err)) { ok = false; break; }
-        uint8_t *vr = v_s + (j % ST) * kTile + jl * 128;
+        if (!wait_warp(sh, &sh.v_full[j % ST], (j / ST) & 1, a.err)) { ok = false; break; }
+        if (key >= L) {
+          uint8_t *vr = v_s + (j % ST) * kTile + jl * 128;
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
+          for (int c = 0; c < 2; ++c)
 #pragma unroll
-          for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4 *>(vr + c * BK * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+            for (int u = 0; u < 8; ++u)
+              *reinterpret_cast<uint4 *>(vr + c * BK * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+        }
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       mbar_arrive(&sh.p_full[j & 1]);
     }
     // epilogue: column sums across the CTA, then O^T / l
-    if (ok && n > 0) ok = wait_bar(sh, &sh.o_done, (n - 1) & 1, a.err);
+    if (ok && n > 0) ok = wait_warp(sh, &sh.o_done, (n - 1) & 1, a.err);
+    ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     if (ok) {
 #pragma unroll
@@ -395,7 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == q) mine = l_part[q];
       if (lane < RP) sh.wsum[w4][lane] = mine;
       mbar_arrive(&sh.grp);
-      ok = wait_bar(sh, &sh.grp, n & 1, a.err);
+      ok = wait_warp(sh, &sh.grp, n & 1, a.err);
     }
     if (ok) {
       uint32_t ou[RP];

@@ -112,6 +112,12 @@ __device__ __forceinline__ bool wait_bar(Shared &sh, uint64_t *bar, uint32_t par
   }
 }
 
+// The same wait taken by a whole warp with one answer, so warp-collective
+// tcgen05 loads/stores that follow are never reached by part of a warp.
+__device__ __forceinline__ bool wait_warp(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
+  return __all_sync(0xffffffffu, wait_bar(sh, bar, parity, err));
+}
+
 template <typename T> struct IsBf16 { static constexpr int v = 0; };
 template <> struct IsBf16<__nv_bfloat16> { static constexpr int v = 1; };
 
@@ -328,7 +334,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
       const int key0 = (n_lo + j) * BN;
       const int sb = NT == 2 ? t : (j & 1);                 // S/P buffer and its barriers
       const uint32_t s_par = NT == 2 ? (j & 1) : ((j >> 1) & 1);
-      if (!wait_bar(sh, &sh.s_full[sb], s_par, a.err)) { ok = false; break; }
+      if (!wait_warp(sh, &sh.s_full[sb], s_par, a.err)) { ok = false; break; }
       tc_fence_after();
       const uint32_t scol = tmem + lane_off + C::kSCol0 + sb * BN;
       float x[BN];
@@ -385,7 +391,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
       tmem_wait_st();
       if (j > 0) {
         // O holds P_{j-1} V_{j-1} once this completes; only then may it be rescaled
-        if (!wait_bar(sh, &sh.o_done[t], (j - 1) & 1, a.err)) { ok = false; break; }
+        if (!wait_warp(sh, &sh.o_done[t], (j - 1) & 1, a.err)) { ok = false; break; }
         tc_fence_after();
         if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
@@ -404,7 +410,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
       mbar_arrive(&sh.p_full[sb]);
     }
     // epilogue: O / l -> dtype, LSE = ln(sum exp(s))
-    if (ok && nt > 0) ok = wait_bar(sh, &sh.o_done[t], (nt - 1) & 1, a.err);
+    if (ok && nt > 0) ok = wait_warp(sh, &sh.o_done[t], (nt - 1) & 1, a.err);
+    ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     if (ok) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
