@@ -132,6 +132,24 @@ def traffic_for(kernel_key):
         return None
 
 
+def max_over_ranks(ms, world, device=None):
+    """The job's step time: the slowest rank's (a MAX all-reduce); with one
+    rank, the local time."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(step_flops, ms, world):
+    """Whole-job TFLOP/s: every rank runs its own replica of the step."""
+    return world * step_flops / (ms * 1e-3) / 1e12
+
+
 def timed(fn, steps, stream):
     import torch
 
@@ -364,11 +382,8 @@ def run_ours(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clk:
         ms = timed(step, args.steps, stream)
     launches = libattn.launch_count() - n0
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * STEP_FLOPS / (ms * 1e-3) / 1e12
+    ms = max_over_ranks(ms, world, device="cuda")
+    value = job_value(STEP_FLOPS, ms, world)
 
     extra_steps = max(5, min(args.steps, 20))
     ms_fwd = timed(fwd, extra_steps, stream)

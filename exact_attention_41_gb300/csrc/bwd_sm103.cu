@@ -95,9 +95,10 @@ __device__ __forceinline__ bool wait_warp(Shared &sh, uint64_t *bar, uint32_t pa
 template <typename T> struct IsBf16 { static constexpr int v = 0; };
 template <> struct IsBf16<__nv_bfloat16> { static constexpr int v = 1; };
 
-struct BwdGeom {
-  int q0, lq, k0, lk, key0, c_lo, nch, n_iter;
-};
+// Fire-and-forget fp32 add to global memory (no value returned).
+__device__ __forceinline__ void red_add(float *p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
 
 // Query chunks [c_lo, c_lo + nch) that can see any key of block nb.
 __device__ __forceinline__ void chunk_range(int nb, int lq, int lk, int win_l, int win_r,
@@ -274,17 +275,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool cap = f.softcap > 0.f;
     const float sl2 = f.scale * kLog2e, cap_in = cap ? f.scale / f.softcap : 0.f;
     bool ok = true;
+    // thread tid fetches element tid % 64 of the LSE (tid < 64) or D (tid >= 64)
+    // of a chunk; the fetch for iteration it+1 is issued during iteration it
+    auto fetch = [&](int it) -> float {
+      if (it >= n_iter) return 0.f;
+      const int h = kvh * g + it / nch;
+      const int i = (c_lo + it % nch) * BQ + (tid & (BQ - 1));
+      if (i >= lq) return 0.f;
+      const int64_t li = f.seqs.lse_index(b, h, q0, i);
+      return tid < BQ ? f.lse[li] * kLog2e : a.dsum[li];
+    };
+    float next = fetch(0);
     for (int it = 0; it < n_iter; ++it) {
       const int buf = it & 1;
-      const int h = kvh * g + it / nch;
       const int i0 = (c_lo + it % nch) * BQ;
-      {
-        const int e = tid & (BQ - 1), i = i0 + e;
-        if (tid < BQ)
-          sh.lse2[buf][e] = i < lq ? f.lse[f.seqs.lse_index(b, h, q0, i)] * kLog2e : 0.f;
-        else
-          sh.dsum[buf][e] = i < lq ? a.dsum[f.seqs.lse_index(b, h, q0, i)] : 0.f;
-      }
+      if (tid < BQ)
+        sh.lse2[buf][tid] = next;
+      else
+        sh.dsum[buf][tid - BQ] = next;
+      next = fetch(it + 1);
       mbar_arrive(&sh.grp_p);  // the chunk's LSE and D are in shared memory
       if (!wait_warp(sh, &sh.grp_p, it & 1, f.err)) { ok = false; break; }
       if (!wait_warp(sh, &sh.sdp_full, it & 1, f.err)) { ok = false; break; }
@@ -421,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int rows = min(BQ, lq - i0);
 #pragma unroll
       for (int e = 0; e < BQ; ++e)
-        if (e < rows) atomicAdd(acc + (int64_t)e * f.hq * D, __uint_as_float(u[e]));
+        if (e < rows) red_add(acc + (int64_t)e * f.hq * D, __uint_as_float(u[e]));
       if (a.deterministic) {
         __threadfence();
         mbar_arrive(&sh.grp_q);  // every add of this key block is performed

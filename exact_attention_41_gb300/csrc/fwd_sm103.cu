@@ -347,6 +347,11 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
 #pragma unroll
         for (int e = 0; e < BN; ++e) x[e] = __uint_as_float(u[e]);
       }
+      // softcap, then the mask (Inference Cookbook FAQ Q22 order)
+      if (cap) {
+#pragma unroll
+        for (int e = 0; e < BN; ++e) x[e] = cap_out * tanhf(x[e] * cap_in);
+      }
       const bool need_mask = key0 < lo_tile_max || key0 + BN - 1 > hi_tile_min;
       if (need_mask) {
 #pragma unroll
@@ -354,10 +359,6 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
           const int kj = key0 + e;
           if (kj < lo_i || kj > hi_i) x[e] = -INFINITY;
         }
-      }
-      if (cap) {
-#pragma unroll
-        for (int e = 0; e < BN; ++e) x[e] = cap_out * tanhf(x[e] * cap_in);
       }
       // raw-score max: scale and softcap preserve the order (scale >= 0)
       float mt = -INFINITY;
