@@ -12,18 +12,20 @@
 // query heads of its GQA group and the 64-row query chunks that can see those
 // keys.  Roles:
 //
-//   warp 0      TMA producer: K and V once, Q and dO chunks into a 2-stage ring.
-//   warp 1      MMA issuer: S^T = K Q^T and dP^T = V dO^T into TMEM, then
-//               dV += P^T dO, dK += dS^T Q (P^T, dS^T from shared memory) and
-//               dQ^T = K^T dS^T into one of two TMEM buffers.
-//   warps 2-5   one thread per key row: P^T and dS^T from S^T, dP^T (TMEM),
-//               the chunk's LSE and D; bf16/fp16 into shared memory for the
-//               MMAs; finally dK and dV out of TMEM.
-//   warps 6-9   one thread per head-dim column: dQ^T out of TMEM, added into
-//               an fp32 dQ accumulator in global memory.  In deterministic
-//               mode the key blocks add to each query chunk in key-block order
-//               (a per-chunk turn counter), so the fp32 sums are bitwise
-//               reproducible (Inference Cookbook FAQ Q11).
+//   warp 0       TMA producer: K and V once, Q and dO chunks into a 3-stage ring.
+//   warp 1       MMA issuer: S^T = K Q^T and dP^T = V dO^T into TMEM, then
+//                dV += P^T dO, dK += dS^T Q and dQ^T = K^T dS^T (P^T and dS^T
+//                from shared memory).
+//   warps 2-9    two warpgroups, one thread per (key row, half of the chunk's
+//                queries): P^T and dS^T from S^T and dP^T, written to shared
+//                memory as a high and a low 16-bit part each, so the dV and dK
+//                products see P and dS to about 16 significant bits; finally
+//                dK and dV out of TMEM.
+//   warps 10-13  one thread per head-dim column: dQ^T out of TMEM, added into
+//                an fp32 accumulator in global memory (`red.global.add`).  In
+//                deterministic mode the key blocks add to each query chunk in
+//                key-block order (a per-chunk turn counter), so the fp32 sums
+//                are bitwise reproducible (Inference Cookbook FAQ Q11).
 //
 // TMEM (512 columns): dV [0,128), dK [128,256), S^T [256,320), dP^T [320,384),
 // dQ^T buffers [384,448) and [448,512).
@@ -42,25 +44,25 @@ using namespace sm103;
 constexpr int D = 128;
 constexpr int BN = 128;   // keys per CTA
 constexpr int BQ = 64;    // query rows per iteration
-constexpr int ST = 2;     // Q/dO ring stages
-constexpr int kThreads = 320;
+constexpr int ST = 3;     // Q/dO ring stages
+constexpr int kThreads = 448;
 constexpr int kTileK = BN * D * 2;       // 32 KB
 constexpr int kChunk = BQ * D * 2;       // 16 KB
 constexpr int kPT = BN * BQ * 2;         // 16 KB
-constexpr int kSmemData = 2 * kTileK + ST * 2 * kChunk + 2 * 2 * kPT;  // 192 KB
+constexpr int kSmemData = 2 * kTileK + ST * 2 * kChunk + 4 * kPT;  // 224 KB
 constexpr int kSmem = kSmemData + 1024;
 constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 320, kColDQ = 384;
 
 struct Shared {
   uint64_t kv_full;
   uint64_t qd_full[ST], qd_empty[ST];
-  uint64_t sdp_full, st_free;
-  uint64_t pds_full[2], mma_done[2], dq_free[2];
-  uint64_t grp_p, grp_q;  // bounded barriers of the P^T warpgroup and the dQ warpgroup
+  uint64_t sdp_full, st_free, pds_full;
+  uint64_t mma_done[2], dq_free[2];
+  uint64_t grp_p[2], grp_q;  // bounded barriers of each P^T warpgroup and of the dQ warpgroup
   uint32_t tmem_base;
   int abort;
-  float lse2[2][BQ];
-  float dsum[2][BQ];
+  float lse2[2][2][BQ / 2];  // [warpgroup][buffer][column]
+  float dsum[2][2][BQ / 2];
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -129,7 +131,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *k_s = smem;
   uint8_t *v_s = smem + kTileK;
   uint8_t *qd_s = smem + 2 * kTileK;           // [stage][Q | dO]
-  uint8_t *pt_s = qd_s + ST * 2 * kChunk;      // [buf][P^T | dS^T]
+  uint8_t *pt_s = qd_s + ST * 2 * kChunk;      // [P high | P low | dS high | dS low], each [key][query]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // CTA -> (key block, kv head, batch): key blocks fastest, so the CTAs of one
@@ -155,13 +157,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.qd_empty[s], 1);
     }
     mbar_init(&sh.sdp_full, 1);
-    mbar_init(&sh.st_free, 128);
+    mbar_init(&sh.st_free, 256);
+    mbar_init(&sh.pds_full, 256);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sh.pds_full[s], 128);
       mbar_init(&sh.mma_done[s], 1);
       mbar_init(&sh.dq_free[s], 128);
+      mbar_init(&sh.grp_p[s], 128);
     }
-    mbar_init(&sh.grp_p, 128);
     mbar_init(&sh.grp_q, 128);
     sh.abort = 0;
     fence_mbar_init();
@@ -241,31 +243,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!issue_sdp(it + 1)) break;
         }
         const int buf = it & 1, st = it % ST;
-        if (!wait_bar(sh, &sh.pds_full[buf], (it >> 1) & 1, f.err)) break;
+        if (!wait_bar(sh, &sh.pds_full, it & 1, f.err)) break;
         tc_fence_after();
         const uint32_t q_a = qd_addr + st * 2 * kChunk, do_a = q_a + kChunk;
-        const uint32_t p_a = pt_addr + buf * 2 * kPT, ds_a = p_a + kPT;
+        const uint32_t ph_a = pt_addr, pl_a = ph_a + kPT, dh_a = pl_a + kPT, dl_a = dh_a + kPT;
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          mma_ss(tmem + kColDV, smem_desc(p_a + kk * 32, 16, 1024),
-                 smem_desc(do_a + kk * 16 * 128, BQ * 128, 1024), id_kv, acc);
-          mma_ss(tmem + kColDK, smem_desc(ds_a + kk * 32, 16, 1024),
-                 smem_desc(q_a + kk * 16 * 128, BQ * 128, 1024), id_kv, acc);
+          const uint64_t do_d = smem_desc(do_a + kk * 16 * 128, BQ * 128, 1024);
+          const uint64_t q_d = smem_desc(q_a + kk * 16 * 128, BQ * 128, 1024);
+          // dV += (P_high + P_low)^T dO,  dK += (dS_high + dS_low)^T Q
+          mma_ss(tmem + kColDV, smem_desc(ph_a + kk * 32, 16, 1024), do_d, id_kv, acc);
+          mma_ss(tmem + kColDV, smem_desc(pl_a + kk * 32, 16, 1024), do_d, id_kv, 1u);
+          mma_ss(tmem + kColDK, smem_desc(dh_a + kk * 32, 16, 1024), q_d, id_kv, acc);
+          mma_ss(tmem + kColDK, smem_desc(dl_a + kk * 32, 16, 1024), q_d, id_kv, 1u);
         }
+        mma_commit(&sh.qd_empty[st]);  // Q and dO of this chunk are no longer read
         if (it >= 2 && !wait_bar(sh, &sh.dq_free[buf], ((it >> 1) - 1) & 1, f.err)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
           mma_ss(tmem + kColDQ + buf * BQ, smem_desc(k_addr + kk * 16 * 128, BN * 128, 1024),
-                 smem_desc(ds_a + kk * 16 * 128, BQ * 128, 1024), id_q, kk > 0);
+                 smem_desc(dh_a + kk * 16 * 128, BQ * 128, 1024), id_q, kk > 0);
         mma_commit(&sh.mma_done[buf]);
-        mma_commit(&sh.qd_empty[st]);
       }
     }
-  } else if (warp < 6) {
+  } else if (warp < 10) {
     // ------------------------------------------------------------ P^T, dS^T
-    const int tid = threadIdx.x - 64;
+    const int sw = (warp - 2) >> 2;         // which half of the chunk's 64 queries
+    const int tid = threadIdx.x - 64 - 128 * sw;
     const int j = 32 * (warp & 3) + lane;  // TMEM lane = key row of the block
     const int kj = key0 + j;
     const uint32_t row_t = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
@@ -275,78 +281,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool cap = f.softcap > 0.f;
     const float sl2 = f.scale * kLog2e, cap_in = cap ? f.scale / f.softcap : 0.f;
     bool ok = true;
-    // thread tid fetches element tid % 64 of the LSE (tid < 64) or D (tid >= 64)
-    // of a chunk; the fetch for iteration it+1 is issued during iteration it
+    // thread tid < 32 fetches the LSE of query column 32*sw + tid of a chunk,
+    // 32 <= tid < 64 its D; the fetch for iteration it+1 is issued during it
     auto fetch = [&](int it) -> float {
-      if (it >= n_iter) return 0.f;
+      if (it >= n_iter || tid >= 64) return 0.f;
       const int h = kvh * g + it / nch;
-      const int i = (c_lo + it % nch) * BQ + (tid & (BQ - 1));
+      const int i = (c_lo + it % nch) * BQ + 32 * sw + (tid & 31);
       if (i >= lq) return 0.f;
       const int64_t li = f.seqs.lse_index(b, h, q0, i);
-      return tid < BQ ? f.lse[li] * kLog2e : a.dsum[li];
+      return tid < 32 ? f.lse[li] * kLog2e : a.dsum[li];
     };
     float next = fetch(0);
     for (int it = 0; it < n_iter; ++it) {
       const int buf = it & 1;
-      const int i0 = (c_lo + it % nch) * BQ;
-      if (tid < BQ)
-        sh.lse2[buf][tid] = next;
-      else
-        sh.dsum[buf][tid - BQ] = next;
+      const int i0 = (c_lo + it % nch) * BQ + 32 * sw;
+      if (tid < 32)
+        sh.lse2[sw][buf][tid] = next;
+      else if (tid < 64)
+        sh.dsum[sw][buf][tid - 32] = next;
       next = fetch(it + 1);
-      mbar_arrive(&sh.grp_p);  // the chunk's LSE and D are in shared memory
-      if (!wait_warp(sh, &sh.grp_p, it & 1, f.err)) { ok = false; break; }
+      mbar_arrive(&sh.grp_p[sw]);  // this half's LSE and D are in shared memory
+      if (!wait_warp(sh, &sh.grp_p[sw], it & 1, f.err)) { ok = false; break; }
       if (!wait_warp(sh, &sh.sdp_full, it & 1, f.err)) { ok = false; break; }
       tc_fence_after();
-      uint32_t su[BQ], du[BQ];
-      tmem_ld32(row_t + kColS, *reinterpret_cast<uint32_t(*)[32]>(su));
-      tmem_ld32(row_t + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
-      tmem_ld32(row_t + kColDP, *reinterpret_cast<uint32_t(*)[32]>(du));
-      tmem_ld32(row_t + kColDP + 32, *reinterpret_cast<uint32_t(*)[32]>(du + 32));
+      uint32_t su[32], du[32];
+      tmem_ld32(row_t + kColS + 32 * sw, su);
+      tmem_ld32(row_t + kColDP + 32 * sw, du);
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive(&sh.st_free);
-      uint32_t pk[BQ / 2], dk[BQ / 2];
-#pragma unroll
-      for (int e = 0; e < BQ; e += 2) {
-        float pv[2], dv[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int i = i0 + e + u;
-          const float s = __uint_as_float(su[e + u]);
-          float x, dcap = 1.f;
-          if (cap) {
-            const float t = tanhf(s * cap_in);
-            x = f.softcap * t * kLog2e;
-            dcap = 1.f - t * t;
-          } else {
-            x = s * sl2;
-          }
-          const bool vis = i >= qlo && i <= qhi;
-          const float p = vis ? ex2(x - sh.lse2[buf][e + u]) : 0.f;
-          pv[u] = p;
-          dv[u] = p * (__uint_as_float(du[e + u]) - sh.dsum[buf][e + u]) * dcap;
-        }
-        pk[e / 2] = Elem<T>::from_f2(pv[0], pv[1]);
-        dk[e / 2] = Elem<T>::from_f2(dv[0], dv[1]);
-      }
-      if (it >= 2 && !wait_warp(sh, &sh.mma_done[buf], ((it >> 1) - 1) & 1, f.err)) {
+      // the MMAs of the previous chunk must be done reading the P/dS buffers
+      if (it >= 1 && !wait_warp(sh, &sh.mma_done[(it - 1) & 1], ((it - 1) >> 1) & 1, f.err)) {
         ok = false;
         break;
       }
-      uint8_t *p_s = pt_s + buf * 2 * kPT, *ds_s = p_s + kPT;
+      // two halves of 16 columns: compute, split into high and low 16-bit
+      // parts, store (each row is 128 bytes; this warpgroup owns 64 of them)
 #pragma unroll
-      for (int cc = 0; cc < 8; ++cc) {
-        const uint32_t off = j * 128 + ((cc ^ (j & 7)) << 4);
-        *reinterpret_cast<uint4 *>(p_s + off) =
-            make_uint4(pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-        *reinterpret_cast<uint4 *>(ds_s + off) =
-            make_uint4(dk[4 * cc], dk[4 * cc + 1], dk[4 * cc + 2], dk[4 * cc + 3]);
+      for (int hv = 0; hv < 2; ++hv) {
+        uint32_t w[4][8];  // [P high, P low, dS high, dS low][8 packed pairs]
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int col = 16 * hv + e + u;
+            const int i = i0 + col;
+            const float s = __uint_as_float(su[col]);
+            float x, dcap = 1.f;
+            if (cap) {
+              const float t = tanhf(s * cap_in);
+              x = f.softcap * t * kLog2e;
+              dcap = 1.f - t * t;
+            } else {
+              x = s * sl2;
+            }
+            const bool vis = i >= qlo && i <= qhi;
+            const float p = vis ? ex2(x - sh.lse2[sw][buf][col]) : 0.f;
+            pv[u] = p;
+            dv[u] = p * (__uint_as_float(du[col]) - sh.dsum[sw][buf][col]) * dcap;
+          }
+          w[0][e / 2] = Elem<T>::from_f2(pv[0], pv[1]);
+          const float2 ph = Elem<T>::to_f2(w[0][e / 2]);
+          w[1][e / 2] = Elem<T>::from_f2(pv[0] - ph.x, pv[1] - ph.y);
+          w[2][e / 2] = Elem<T>::from_f2(dv[0], dv[1]);
+          const float2 dh = Elem<T>::to_f2(w[2][e / 2]);
+          w[3][e / 2] = Elem<T>::from_f2(dv[0] - dh.x, dv[1] - dh.y);
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const int chunk = 4 * sw + 2 * hv + cc;  // 16-byte chunk of the 128-byte row
+            const uint32_t off = j * 128 + ((chunk ^ (j & 7)) << 4);
+            *reinterpret_cast<uint4 *>(pt_s + m * kPT + off) =
+                make_uint4(w[m][4 * cc], w[m][4 * cc + 1], w[m][4 * cc + 2], w[m][4 * cc + 3]);
+          }
+        }
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(&sh.pds_full[buf]);
+      mbar_arrive(&sh.pds_full);
     }
-    // dK, dV out of TMEM
+    // dK, dV out of TMEM: each warpgroup writes half of the head-dim columns
     if (ok && n_iter > 0)
       ok = wait_warp(sh, &sh.mma_done[(n_iter - 1) & 1], ((n_iter - 1) >> 1) & 1, f.err);
     ok = __all_sync(0xffffffffu, ok);
@@ -357,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       T *dvr = static_cast<T *>(a.dv) + off;
       T *dkr = static_cast<T *>(a.dk) + off;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 2 * sw; c < 2 * sw + 2; ++c) {
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           uint32_t u[32];
@@ -384,9 +400,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------ dQ
-    const int tid = threadIdx.x - 192;
+    const int tid = threadIdx.x - 320;
     const int dl = 32 * (warp & 3) + lane;  // TMEM lane = head-dim column
     const uint32_t row_t = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
+    uint32_t grp_phase = 0;
+    auto group_sync = [&]() -> bool {
+      mbar_arrive(&sh.grp_q);
+      return wait_warp(sh, &sh.grp_q, (grp_phase++) & 1, f.err);
+    };
     for (int it = 0; it < n_iter; ++it) {
       const int buf = it & 1;
       const int h = kvh * g + it / nch;
@@ -423,8 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        mbar_arrive(&sh.grp_q);  // thread 0 has seen this key block's turn
-        if (!wait_warp(sh, &sh.grp_q, 0, f.err)) break;
+        if (!group_sync()) break;  // thread 0 has seen this key block's turn
       }
       float *acc = a.dq_acc + ((int64_t)(q0 + i0) * f.hq + h) * D + dl;
       const int rows = min(BQ, lq - i0);
@@ -433,8 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (e < rows) red_add(acc + (int64_t)e * f.hq * D, __uint_as_float(u[e]));
       if (a.deterministic) {
         __threadfence();
-        mbar_arrive(&sh.grp_q);  // every add of this key block is performed
-        if (!wait_warp(sh, &sh.grp_q, 1, f.err)) break;
+        if (!group_sync()) break;  // every add of this key block is performed
         if (tid == 0) atomicAdd(turn_ctr, 1);
       }
     }

@@ -137,8 +137,20 @@ __global__ void __launch_bounds__(32) combine_kernel(DecodeArgs a) {
   const int r = blockIdx.x, h = blockIdx.y, bi = blockIdx.z;
   const int64_t stride_l = (int64_t)a.b * a.hq * a.sq;
   const int64_t li = ((int64_t)bi * a.hq + h) * a.sq + r;
+  // splits whose key range holds no key any query row may see were not
+  // written (same test as the split kernels); they are skipped
+  const int L = a.cache_seqlens[bi] + a.s_new;
+  int lo0, hi0, lo1, hi1;
+  key_range(0, a.sq, L, a.win_l, a.win_r, lo0, hi0);
+  key_range(a.sq - 1, a.sq, L, a.win_l, a.win_r, lo1, hi1);
+  auto used = [&](int s) {
+    const int kb = max(lo0, s * a.split_chunk);
+    const int ke = min(hi1 + 1, min(L, (s + 1) * a.split_chunk));
+    return ke > kb;
+  };
   float m = -INFINITY;
-  for (int s = lane; s < a.num_splits; s += 32) m = fmaxf(m, a.lse_part[s * stride_l + li]);
+  for (int s = lane; s < a.num_splits; s += 32)
+    if (used(s)) m = fmaxf(m, a.lse_part[s * stride_l + li]);
   m = warp_max(m);
   float acc[V];
 #pragma unroll
@@ -148,6 +160,7 @@ __global__ void __launch_bounds__(32) combine_kernel(DecodeArgs a) {
     const int64_t stride_o = (int64_t)a.b * a.sq * a.hq * D;
     const int64_t oi = (((int64_t)bi * a.sq + r) * a.hq + h) * D + lane * V;
     for (int s = 0; s < a.num_splits; ++s) {
+      if (!used(s)) continue;
       const float w = exp2f((a.lse_part[s * stride_l + li] - m) * kLog2e);
       if (w == 0.f) continue;
       wsum += w;

@@ -155,6 +155,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int k_end = min(hi1 + 1, min(L, (split + 1) * a.split_chunk));  // exclusive
   const int t_first = k_begin / BK;
   const int n = k_end > k_begin ? (k_end - 1) / BK - t_first + 1 : 0;
+  // an empty split writes nothing: the combine step skips it by the same test
+  if (n == 0 && a.num_splits > 1) return;
 
   if (threadIdx.x == 0) {
     mbar_init(&sh.q_full, 1);

@@ -360,10 +360,15 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
           if (kj < lo_i || kj > hi_i) x[e] = -INFINITY;
         }
       }
-      // raw-score max: scale and softcap preserve the order (scale >= 0)
-      float mt = -INFINITY;
+      // raw-score max: scale and softcap preserve the order (scale >= 0);
+      // eight independent partial maxima keep the dependency chains short
+      float mp[8];
 #pragma unroll
-      for (int e = 0; e < BN; ++e) mt = fmaxf(mt, x[e]);
+      for (int u = 0; u < 8; ++u) mp[u] = x[u];
+#pragma unroll
+      for (int e = 8; e < BN; ++e) mp[e & 7] = fmaxf(mp[e & 7], x[e]);
+      const float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
       const float f = cap ? 1.f : sl2;  // x * f is the score in log2 units
       const float m_new = fmaxf(m_ref, mt * f);
       const bool rescale = m_new > m_ref + kRescaleThreshold;
@@ -374,7 +379,9 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
         m_ref = m_new;
       }
       const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-      float rs0 = 0.f, rs1 = 0.f;
+      float rs[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) rs[u] = 0.f;
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t pk[16];
@@ -382,13 +389,13 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
         for (int e = 0; e < 16; ++e) {
           const float p0 = ex2(fmaf(x[c * 32 + 2 * e], f, neg_m));
           const float p1 = ex2(fmaf(x[c * 32 + 2 * e + 1], f, neg_m));
-          rs0 += p0;
-          rs1 += p1;
+          rs[(2 * e) & 7] += p0;
+          rs[(2 * e + 1) & 7] += p1;
           pk[e] = pack2<T>(p0, p1);
         }
         tmem_st16(scol + c * 16, pk);
       }
-      l += rs0 + rs1;
+      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       tmem_wait_st();
       if (j > 0) {
         // O holds P_{j-1} V_{j-1} once this completes; only then may it be rescaled
