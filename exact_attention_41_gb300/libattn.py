@@ -38,6 +38,8 @@ _SIGS = {
     "attn_kvcache_workspace_size": ([_i] * 7, _sz),
     "attn_fwd_kvcache": ([_vp] * 7 + [_i] * 3 + [_vp, _vp] + [_i] * 7 +
                          [_f, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
+    "attn_fwd_kvcache_noalloc": ([_vp] * 7 + [_i] * 3 + [_vp, _vp] + [_i] * 7 +
+                                 [_f, _i, _i, _i, _f, _i, _vp], _i),
     "attn_get_device_error": ([_vp, ctypes.POINTER(_i)], _i),
     "attn_launch_count": ([], ctypes.c_ulonglong),
 }

@@ -178,6 +178,32 @@ attn_status attn_fwd_kvcache(const void *q, void *k_cache, void *v_cache, const 
                              void *workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * attn_fwd_kvcache_noalloc -- the decode of attn_fwd_kvcache for callers
+ * that cannot allocate device memory.  The pages have no counterpart; it
+ * exists for hosts such as code that runs while a CUDA graph is being
+ * captured (cudaMalloc cannot be captured), inference-server plugins whose
+ * device memory belongs to a pool they may not grow, and plain C callers
+ * without a CUDA allocator.  Arguments and results are those of
+ * attn_fwd_kvcache without `workspace`: the split partials go to a 32 MiB
+ * array inside the library (held on every GPU that loads the library until
+ * the process exits).  A call whose attn_kvcache_workspace_size(...) exceeds
+ * 32 MiB returns ATTN_ERR_WORKSPACE and launches nothing.  Nothing is
+ * allocated or freed.  The first call on a device looks up the array's
+ * device address (a host-side query, once per device); make that first call
+ * before any stream capture.  All calls share the one array: calls that
+ * overlap on the GPU (different streams, or several threads) race on it and
+ * must be serialised by the caller.
+ */
+attn_status attn_fwd_kvcache_noalloc(const void *q, void *k_cache, void *v_cache,
+                                     const void *k_new, const void *v_new,
+                                     const int32_t *cache_seqlens, const int32_t *block_table,
+                                     int num_pages, int page_size, int max_pages_per_seq,
+                                     void *out, float *lse, int dtype, int b, int sq, int s_new,
+                                     int hq, int hkv, int d, float scale, int causal, int win_l,
+                                     int win_r, float softcap, int num_splits,
+                                     attn_stream_t stream);
+
+/*
  * Reads and clears the sticky device error word of the current device
  * (synchronises `stream`; diagnostic use, not for the hot path).  Returns
  * ATTN_OK, ATTN_ERR_DEVICE or ATTN_ERR_TIMEOUT.  If `detail` is not NULL it
