@@ -8,7 +8,8 @@
 //   warp 1      MMA issuer (one elected lane): S_j = Q K_j^T into TMEM,
 //               O += P_j V_j with P_j read from TMEM; also owns the TMEM
 //               allocation.
-//   warps 2-5   softmax warpgroup, one thread per query row: loads S_j from
+//   softmax     one warpgroup per 128-row query tile (warps 4-11 for two
+//               tiles, 2-5 for one), one thread per query row: loads S_j from
 //               TMEM, applies scale -> softcap -> mask (Inference Cookbook
 //               FAQ Q22 order; bottom-right causal FAQ Q6; window FAQ Q21),
 //               runs the online max/sum update, writes P_j (fp16/bf16) back
@@ -76,7 +77,10 @@ struct FwdCfg {
   static constexpr int kSmem = (kSmemData + 1024 > 120 * 1024 ? kSmemData + 1024 : 120 * 1024);
   static constexpr int kSCol0 = NT * D;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kThreads = 64 + 128 * NT;
+  // NT = 2: warpgroup 0 = producer, MMA and two idle warps; warpgroups 1-2 =
+  // softmax.  NT = 1: warps 0-1 = producer, MMA; warps 2-5 = softmax.
+  static constexpr int kThreads = NT == 2 ? 384 : 192;
+  static constexpr int kSoftmaxWarp0 = NT == 2 ? 4 : 2;
   static_assert(NT * D + 2 * BN <= 512, "TMEM budget");
 };
 
@@ -185,7 +189,13 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
-
+  // NT = 2 is launched at 168 registers a thread (12 warps).  The producer/MMA
+  // warpgroup gives registers to the softmax warpgroups, which hold a whole
+  // 128-score row: 128 * 64 + 256 * 216 <= 384 * 168.  Each setmaxnreg sits at
+  // the head of its warpgroup's branch, so every role's code is compiled for
+  // its own register budget.
+  if (warp < C::kSoftmaxWarp0) {
+  if constexpr (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (elect_one()) {
@@ -312,9 +322,11 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
         }
       }
     }
+  }
   } else {
+    if constexpr (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
     // ------------------------------------------------------------ softmax
-    const int t = (warp - 2) >> 2;         // query tile of this warpgroup
+    const int t = (warp - C::kSoftmaxWarp0) >> 2;  // query tile of this warpgroup
     const int r = 32 * (warp & 3) + lane;  // TMEM lane = query row in the tile
     const int i = m0 + t * kBM + r;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
