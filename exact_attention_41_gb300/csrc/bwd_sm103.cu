@@ -219,19 +219,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_q = idesc_f16(128, BQ, ab, 1, 1);   // dQ^T (A = K^T, B = dS^T)
       const uint32_t k_addr = smem_u32(k_s), v_addr = smem_u32(v_s);
       const uint32_t qd_addr = smem_u32(qd_s), pt_addr = smem_u32(pt_s);
+      // descriptor bases; every operand below is base + constant offset
+      const uint64_t k_kd = smem_desc(k_addr, 16, 1024), v_kd = smem_desc(v_addr, 16, 1024);
+      const uint64_t k_mn = smem_desc(k_addr, BN * 128, 1024);
+      const uint64_t qd_k = smem_desc(qd_addr, 16, 1024), qd_mn = smem_desc(qd_addr, BQ * 128, 1024);
+      const uint64_t pt_k = smem_desc(pt_addr, 16, 1024), pt_mn = smem_desc(pt_addr, BQ * 128, 1024);
       auto issue_sdp = [&](int it) -> bool {
         const int st = it % ST;
         if (!wait_bar(sh, &sh.qd_full[st], (it / ST) & 1, f.err)) return false;
         tc_fence_after();
-        const uint32_t q_a = qd_addr + st * 2 * kChunk, do_a = q_a + kChunk;
+        const uint32_t q_o = st * 2 * kChunk, do_o = q_o + kChunk;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
           const uint32_t qo = (kk / 4) * (BQ * 128) + (kk % 4) * 32;
-          mma_ss(tmem + kColS, smem_desc(k_addr + ko, 16, 1024), smem_desc(q_a + qo, 16, 1024),
-                 id_s, kk > 0);
-          mma_ss(tmem + kColDP, smem_desc(v_addr + ko, 16, 1024),
-                 smem_desc(do_a + qo, 16, 1024), id_s, kk > 0);
+          mma_ss(tmem + kColS, desc_add(k_kd, ko), desc_add(qd_k, q_o + qo), id_s, kk > 0);
+          mma_ss(tmem + kColDP, desc_add(v_kd, ko), desc_add(qd_k, do_o + qo), id_s, kk > 0);
         }
         mma_commit(&sh.sdp_full);
         return true;
@@ -245,26 +248,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int buf = it & 1, st = it % ST;
         if (!wait_bar(sh, &sh.pds_full, it & 1, f.err)) break;
         tc_fence_after();
-        const uint32_t q_a = qd_addr + st * 2 * kChunk, do_a = q_a + kChunk;
-        const uint32_t ph_a = pt_addr, pl_a = ph_a + kPT, dh_a = pl_a + kPT, dl_a = dh_a + kPT;
+        const uint32_t q_o = st * 2 * kChunk, do_o = q_o + kChunk;
 #pragma unroll
         for (int kk = 0; kk < BQ / 16; ++kk) {
           const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          const uint64_t do_d = smem_desc(do_a + kk * 16 * 128, BQ * 128, 1024);
-          const uint64_t q_d = smem_desc(q_a + kk * 16 * 128, BQ * 128, 1024);
+          const uint64_t do_d = desc_add(qd_mn, do_o + kk * 16 * 128);
+          const uint64_t q_d = desc_add(qd_mn, q_o + kk * 16 * 128);
           // dV += (P_high + P_low)^T dO,  dK += (dS_high + dS_low)^T Q
-          mma_ss(tmem + kColDV, smem_desc(ph_a + kk * 32, 16, 1024), do_d, id_kv, acc);
-          mma_ss(tmem + kColDV, smem_desc(pl_a + kk * 32, 16, 1024), do_d, id_kv, 1u);
-          mma_ss(tmem + kColDK, smem_desc(dh_a + kk * 32, 16, 1024), q_d, id_kv, acc);
-          mma_ss(tmem + kColDK, smem_desc(dl_a + kk * 32, 16, 1024), q_d, id_kv, 1u);
+          mma_ss(tmem + kColDV, desc_add(pt_k, 0 * kPT + kk * 32), do_d, id_kv, acc);
+          mma_ss(tmem + kColDV, desc_add(pt_k, 1 * kPT + kk * 32), do_d, id_kv, 1u);
+          mma_ss(tmem + kColDK, desc_add(pt_k, 2 * kPT + kk * 32), q_d, id_kv, acc);
+          mma_ss(tmem + kColDK, desc_add(pt_k, 3 * kPT + kk * 32), q_d, id_kv, 1u);
         }
         mma_commit(&sh.qd_empty[st]);  // Q and dO of this chunk are no longer read
         if (it >= 2 && !wait_bar(sh, &sh.dq_free[buf], ((it >> 1) - 1) & 1, f.err)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ss(tmem + kColDQ + buf * BQ, smem_desc(k_addr + kk * 16 * 128, BN * 128, 1024),
-                 smem_desc(dh_a + kk * 16 * 128, BQ * 128, 1024), id_q, kk > 0);
+          mma_ss(tmem + kColDQ + buf * BQ, desc_add(k_mn, kk * 16 * 128),
+                 desc_add(pt_mn, 2 * kPT + kk * 16 * 128), id_q, kk > 0);
         mma_commit(&sh.mma_done[buf]);
       }
     }

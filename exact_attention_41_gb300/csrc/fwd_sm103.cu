@@ -241,24 +241,25 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
       constexpr uint32_t id_s = idesc_f16(kBM, BN, ab, 0, 0);
       constexpr uint32_t id_o = idesc_f16(kBM, D, ab, 0, 1);
       const uint32_t q_addr = smem_u32(q_s), k_addr = smem_u32(k_s), v_addr = smem_u32(v_s);
+      // descriptor bases; every operand below is base + constant offset
+      const uint64_t q_d = smem_desc(q_addr, 16, 1024), k_d = smem_desc(k_addr, 16, 1024);
+      const uint64_t v_d = smem_desc(v_addr, BN * 128, 1024);
       // S_t = Q_t K_j^T into TMEM column `dcol`
       auto mma_s = [&](int t, int j, uint32_t dcol) {
-        const int st = j % ST;
+        const uint32_t ko = (j % ST) * C::kKVBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t ad = smem_desc(
-              q_addr + t * C::kQBytes + (kk / 4) * (kBM * 128) + (kk % 4) * 32, 16, 1024);
-          const uint64_t bd = smem_desc(k_addr + st * C::kKVBytes + (kk / 4) * (BN * 128) +
-                                            (kk % 4) * 32, 16, 1024);
+          const uint64_t ad = desc_add(q_d, t * C::kQBytes + (kk / 4) * (kBM * 128) + (kk % 4) * 32);
+          const uint64_t bd = desc_add(k_d, ko + (kk / 4) * (BN * 128) + (kk % 4) * 32);
           mma_ss(dcol, ad, bd, id_s, kk > 0);
         }
       };
       // O_t += P V_j with P read from TMEM column `pcol`
       auto mma_pv = [&](int t, int j, uint32_t pcol) {
-        const int st = j % ST;
+        const uint32_t vo = (j % ST) * C::kKVBytes;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
-          const uint64_t bd = smem_desc(v_addr + st * C::kKVBytes + kk * 16 * 128, BN * 128, 1024);
+          const uint64_t bd = desc_add(v_d, vo + kk * 16 * 128);
           mma_ts(tmem + t * D, pcol + kk * 8, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
         }
       };

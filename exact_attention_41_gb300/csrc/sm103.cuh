@@ -139,6 +139,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
+// A descriptor whose start address is `byte_off` bytes further.  Shared
+// memory addresses are below 256 KB, so (address >> 4) fits the 14-bit field
+// and the addition never carries into the other fields.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t byte_off) {
+  return d + (uint64_t)(byte_off >> 4);
+}
+
 // Instruction descriptor for kind::f16: f32 accumulator, A/B both f16
 // (ab_bf16 = 0) or both bf16 (ab_bf16 = 1), A/B major-ness (0 = K-major,
 // 1 = MN-major), N >> 3 at bits 17-22 and M >> 4 at bits 24-28.
