@@ -102,6 +102,23 @@ __device__ __forceinline__ void red_add(float *p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
+// x = hi + lo with hi, lo 16-bit: packed pairs of the high parts and of the
+// low parts.  bf16: hi is x with its low 16 bits cleared (truncation), so
+// lo = x - hi is exact in fp32 and only lo is rounded; fp16: hi rounded to
+// nearest, lo the rounded remainder.
+template <typename T>
+__device__ __forceinline__ void split_hi_lo(const float (&x)[2], uint32_t &hi, uint32_t &lo) {
+  if constexpr (IsBf16<T>::v) {
+    const uint32_t a = __float_as_uint(x[0]) & 0xFFFF0000u, b = __float_as_uint(x[1]) & 0xFFFF0000u;
+    hi = __byte_perm(a, b, 0x7632);  // high halves of a and b -> (a, b) packed
+    lo = Elem<T>::from_f2(x[0] - __uint_as_float(a), x[1] - __uint_as_float(b));
+  } else {
+    hi = Elem<T>::from_f2(x[0], x[1]);
+    const float2 h = Elem<T>::to_f2(hi);
+    lo = Elem<T>::from_f2(x[0] - h.x, x[1] - h.y);
+  }
+}
+
 // Query chunks [c_lo, c_lo + nch) that can see any key of block nb.
 __device__ __forceinline__ void chunk_range(int nb, int lq, int lk, int win_l, int win_r,
                                             int &c_lo, int &nch) {
@@ -343,12 +360,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             pv[u] = p;
             dv[u] = p * (__uint_as_float(du[col]) - sh.dsum[sw][buf][col]) * dcap;
           }
-          w[0][e / 2] = Elem<T>::from_f2(pv[0], pv[1]);
-          const float2 ph = Elem<T>::to_f2(w[0][e / 2]);
-          w[1][e / 2] = Elem<T>::from_f2(pv[0] - ph.x, pv[1] - ph.y);
-          w[2][e / 2] = Elem<T>::from_f2(dv[0], dv[1]);
-          const float2 dh = Elem<T>::to_f2(w[2][e / 2]);
-          w[3][e / 2] = Elem<T>::from_f2(dv[0] - dh.x, dv[1] - dh.y);
+          split_hi_lo<T>(pv, w[0][e / 2], w[1][e / 2]);
+          split_hi_lo<T>(dv, w[2][e / 2], w[3][e / 2]);
         }
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
