@@ -22,10 +22,10 @@
 //                products see P and dS to about 16 significant bits; finally
 //                dK and dV out of TMEM.
 //   warps 10-13  one thread per head-dim column: dQ^T out of TMEM, added into
-//                an fp32 accumulator in global memory (`red.global.add`).  In
-//                deterministic mode the key blocks add to each query chunk in
-//                key-block order (a per-chunk turn counter), so the fp32 sums
-//                are bitwise reproducible (Inference Cookbook FAQ Q11).
+//                an fp32 accumulator in global memory (`red.global.add`).
+//                In deterministic mode (Inference Cookbook FAQ Q11) this
+//                kernel skips dQ and the query-stationary kernel of
+//                bwd_dq_sm103.cu computes it without atomics.
 //
 // TMEM (512 columns): dV [0,128), dK [128,256), S^T [256,320), dP^T [320,384),
 // dQ^T buffers [384,448) and [448,512).
@@ -166,6 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   int c_lo, nch;
   chunk_range(nb, lq, lk, f.win_l, f.win_r, c_lo, nch);
   const int n_iter = g * nch;
+  // deterministic mode: dQ comes from the query-stationary kernel instead
+  const bool with_dq = !a.deterministic;
 
   if (threadIdx.x == 0) {
     mbar_init(&sh.kv_full, 1);
@@ -278,12 +280,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss(tmem + kColDK, desc_add(pt_k, 3 * kPT + kk * 32), q_d, id_kv, 1u);
         }
         mma_commit(&sh.qd_empty[st]);  // Q and dO of this chunk are no longer read
-        if (it >= 2 && !wait_bar(sh, &sh.dq_free[buf], ((it >> 1) - 1) & 1, f.err)) break;
-        tc_fence_after();
+        if (with_dq) {
+          if (it >= 2 && !wait_bar(sh, &sh.dq_free[buf], ((it >> 1) - 1) & 1, f.err)) break;
+          tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk)
-          mma_ss(tmem + kColDQ + buf * BQ, desc_add(k_mn, kk * 16 * 128),
-                 desc_add(pt_mn, 2 * kPT + kk * 16 * 128), id_q, kk > 0);
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ss(tmem + kColDQ + buf * BQ, desc_add(k_mn, kk * 16 * 128),
+                   desc_add(pt_mn, 2 * kPT + kk * 16 * 128), id_q, kk > 0);
+        }
         mma_commit(&sh.mma_done[buf]);
       }
     }
@@ -413,6 +417,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+  } else if (!with_dq) {
+    // dQ warpgroup idle: the query-stationary kernel computes dQ
   } else {
     // ------------------------------------------------------------ dQ
     const int tid = threadIdx.x - 320;
@@ -496,7 +502,8 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int *sem, int6
     load_vec<T, 4>(static_cast<const T *>(a.dout) + off, g);
     float s = o[0] * g[0] + o[1] * g[1] + o[2] * g[2] + o[3] * g[3];
     s = warp_sum(s);
-    reinterpret_cast<float4 *>(a.dq_acc + off)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!a.deterministic)
+      reinterpret_cast<float4 *>(a.dq_acc + off)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (lane == 0) {
       int64_t li;
       if (f.seqs.cu_q) {
@@ -557,7 +564,11 @@ cudaError_t bwd_tc(const BwdArgs &a, int *sem, int sem_per_head, int sms, cudaSt
     if (e == cudaSuccess) e = cudaMemsetAsync(a.dv, 0, bytes, st);
     if (e != cudaSuccess) return e;
   }
-  if (rows_q > 0) {
+  if (a.deterministic) {
+    // dQ from the query-stationary kernel: no atomics, the same bits every run
+    cudaError_t e = launch_bwd_dq_tc(a, st);
+    if (e != cudaSuccess) return e;
+  } else if (rows_q > 0) {
     const int64_t n4 = rows_q * f.hq * D / 4;
     const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, (int64_t)sms * 16);
     bwd_dq_convert_kernel<T><<<std::max(blocks, 1), 256, 0, st>>>(a, n4);

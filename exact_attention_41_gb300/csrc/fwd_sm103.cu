@@ -198,7 +198,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
   if constexpr (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (elect_one()) {
+    // (no key tile visible: nothing is loaded, so no copy outlives the CTA)
+    if (elect_one() && nt > 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);

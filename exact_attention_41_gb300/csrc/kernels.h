@@ -50,6 +50,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // 3-D (rows, heads, d) tensor map, box {64, 1, box_rows}, 128-byte swizzle.
 bool make_map_3d(CUtensorMap *m, const void *base, int dtype, int64_t rows, int heads, int d,
                  int box_rows);
+// dQ of the backward, query-stationary (d = 128): written once, no atomics.
+cudaError_t launch_bwd_dq_tc(const BwdArgs &a, cudaStream_t st);
 // Tensor-core decode; cudaErrorNotSupported for shapes it does not handle.
 cudaError_t launch_decode_tc(const DecodeArgs &a, cudaStream_t st);
 
