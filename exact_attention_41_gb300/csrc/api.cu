@@ -60,15 +60,12 @@ attn_status check_common(int dtype, int hq, int hkv, int d, float scale, int win
 
 attn_status launched(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
-// Turn counters per query head: one per 64-row query chunk of every
-// sequence (chunk c of sequence b at index cu_q[b]/64 + b + c).
-int64_t sem_per_head(int64_t rows, int batch) { return rows / 64 + batch + 1; }
-
 // Backward workspace for `rows` query rows in total: D_i (fp32, LSE
-// layout), the fp32 dQ accumulator, and the turn counters.
-size_t bwd_ws_bytes(int64_t rows, int hq, int d, int batch) {
-  return align256(sizeof(float) * rows * hq) + align256(sizeof(float) * rows * hq * d) +
-         align256(sizeof(int) * sem_per_head(rows, batch) * hq);
+// layout) and, unless deterministic, the fp32 dQ accumulator of the
+// key-stationary kernel's atomic adds.
+size_t bwd_ws_bytes(int64_t rows, int hq, int d, int deterministic) {
+  return align256(sizeof(float) * rows * hq) +
+         (deterministic ? 0 : align256(sizeof(float) * rows * hq * d));
 }
 
 // Splits a backward workspace and launches the backward kernels.
@@ -78,11 +75,8 @@ attn_status run_bwd(BwdArgs &a, int64_t rows, void *workspace, const DeviceInfo 
   const int hq = a.f.hq;
   a.dsum = reinterpret_cast<float *>(ws);
   ws += align256(sizeof(float) * rows * hq);
-  a.dq_acc = reinterpret_cast<float *>(ws);
-  ws += align256(sizeof(float) * rows * hq * a.f.d);
-  int *sem = reinterpret_cast<int *>(ws);
-  if (a.f.d == 128)
-    return launched(launch_bwd_tc(a, sem, (int)sem_per_head(rows, a.f.batch), di->sms, stream));
+  a.dq_acc = a.deterministic ? nullptr : reinterpret_cast<float *>(ws);
+  if (a.f.d == 128) return launched(launch_bwd_tc(a, di->sms, stream));
   return launched(launch_bwd_simt(a, stream));
 }
 
@@ -146,9 +140,9 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *out, flo
 }
 
 size_t attn_bwd_workspace_size(int b, int sq, int sk, int hq, int hkv, int d, int deterministic) {
-  (void)sk; (void)hkv; (void)deterministic;
+  (void)sk; (void)hkv;
   if (b <= 0 || sq <= 0 || hq <= 0 || d <= 0) return 0;
-  return bwd_ws_bytes((int64_t)b * sq, hq, d, b);
+  return bwd_ws_bytes((int64_t)b * sq, hq, d, deterministic);
 }
 
 attn_status attn_bwd(const void *q, const void *k, const void *v, const void *out,
@@ -207,9 +201,9 @@ attn_status attn_fwd_varlen(const void *q, const void *k, const void *v, void *o
 size_t attn_bwd_varlen_workspace_size(int batch, int max_seqlen_q, int max_seqlen_k,
                                       int total_q, int total_k, int hq, int hkv, int d,
                                       int deterministic) {
-  (void)max_seqlen_q; (void)max_seqlen_k; (void)total_k; (void)hkv; (void)deterministic;
+  (void)max_seqlen_q; (void)max_seqlen_k; (void)total_k; (void)hkv;
   if (batch <= 0 || total_q <= 0 || hq <= 0 || d <= 0) return 0;
-  return bwd_ws_bytes(total_q, hq, d, batch);
+  return bwd_ws_bytes(total_q, hq, d, deterministic);
 }
 
 attn_status attn_bwd_varlen(const void *q, const void *k, const void *v, const void *out,

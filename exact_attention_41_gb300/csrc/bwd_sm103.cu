@@ -10,25 +10,33 @@
 //
 // One CTA owns a block of 128 keys of one (batch, KV head) and loops over the
 // query heads of its GQA group and the 64-row query chunks that can see those
-// keys.  Roles:
+// keys.  Two chunks are in flight: chunk `it` uses TMEM buffer it % 2 and is
+// handled by softmax warpgroup it % 2, so one chunk's exponentials overlap
+// the other chunk's matrix products.  Roles (16 warps):
 //
-//   warp 0       TMA producer: K and V once, Q and dO chunks into a 3-stage ring.
-//   warp 1       MMA issuer: S^T = K Q^T and dP^T = V dO^T into TMEM, then
-//                dV += P^T dO, dK += dS^T Q and dQ^T = K^T dS^T (P^T and dS^T
-//                from shared memory).
-//   warps 2-9    two warpgroups, one thread per (key row, half of the chunk's
-//                queries): P^T and dS^T from S^T and dP^T, written to shared
-//                memory as a high and a low 16-bit part each, so the dV and dK
-//                products see P and dS to about 16 significant bits; finally
-//                dK and dV out of TMEM.
-//   warps 10-13  one thread per head-dim column: dQ^T out of TMEM, added into
-//                an fp32 accumulator in global memory (`red.global.add`).
-//                In deterministic mode (Inference Cookbook FAQ Q11) this
-//                kernel skips dQ and the query-stationary kernel of
-//                bwd_dq_sm103.cu computes it without atomics.
+//   warp 0         TMA producer: K and V once, Q and dO chunks into a 3-stage
+//                  ring.
+//   warp 1         MMA issuer and TMEM owner: S^T = K Q^T and dP^T = V dO^T
+//                  into the chunk's buffer; then dQ^T = K^T dS^T into the dP^T
+//                  columns (already read), dV += P^T dO with P^T read from
+//                  TMEM, dK += dS^T Q with dS^T from shared memory.
+//   warps 4-7,     one softmax warpgroup per buffer, one thread per key row:
+//   warps 8-11     P^T and dS^T of the row's 64 queries, each split into a
+//                  high and a low 16-bit part (so the dV and dK products see
+//                  P and dS to about 16 significant bits); P^T goes back into
+//                  the S^T columns, dS^T into shared memory.  At the end each
+//                  warpgroup writes half of the dK and dV columns.
+//   warps 12-15    one thread per head-dim column: dQ^T out of TMEM, added
+//                  into an fp32 accumulator in global memory
+//                  (`red.global.add`).  In deterministic mode (Inference
+//                  Cookbook FAQ Q11) this kernel skips dQ and the
+//                  query-stationary kernel of bwd_dq_sm103.cu computes it
+//                  without atomics.
 //
-// TMEM (512 columns): dV [0,128), dK [128,256), S^T [256,320), dP^T [320,384),
-// dQ^T buffers [384,448) and [448,512).
+// TMEM (512 columns): dV [0,128), dK [128,256), buffer b at 256 + 128 b:
+// S^T, then P^T high/low, in [0,64); dP^T, then dQ^T, in [64,128).  The MMAs
+// of one thread run in issue order, so the products that read P^T from a
+// buffer finish before the next S^T overwrites it.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -43,26 +51,28 @@ using namespace sm103;
 
 constexpr int D = 128;
 constexpr int BN = 128;   // keys per CTA
-constexpr int BQ = 64;    // query rows per iteration
+constexpr int BQ = 64;    // query rows per chunk
 constexpr int ST = 3;     // Q/dO ring stages
-constexpr int kThreads = 448;
+constexpr int kThreads = 512;
 constexpr int kTileK = BN * D * 2;       // 32 KB
 constexpr int kChunk = BQ * D * 2;       // 16 KB
-constexpr int kPT = BN * BQ * 2;         // 16 KB
-constexpr int kSmemData = 2 * kTileK + ST * 2 * kChunk + 4 * kPT;  // 224 KB
+constexpr int kDS = BN * BQ * 2;         // 16 KB: one 16-bit [key][query] array
+constexpr int kSmemData = 2 * kTileK + ST * 2 * kChunk + 2 * 2 * kDS;  // 224 KB
 constexpr int kSmem = kSmemData + 1024;
-constexpr uint32_t kColDV = 0, kColDK = 128, kColS = 256, kColDP = 320, kColDQ = 384;
+constexpr uint32_t kColDV = 0, kColDK = 128, kColBuf = 256;
 
 struct Shared {
   uint64_t kv_full;
   uint64_t qd_full[ST], qd_empty[ST];
-  uint64_t sdp_full, st_free, pds_full;
-  uint64_t mma_done[2], dq_free[2];
-  uint64_t grp_p[2], grp_q;  // bounded barriers of each P^T warpgroup and of the dQ warpgroup
+  uint64_t sdp_full[2];  // S^T, dP^T of the buffer's chunk are in TMEM
+  uint64_t pds_full[2];  // its P^T (TMEM) and dS^T (shared memory) are written
+  uint64_t dq_full[2], dq_free[2];
+  uint64_t all_done;     // every MMA of the CTA has completed
+  uint64_t grp[2];       // bounded barrier of each softmax warpgroup
   uint32_t tmem_base;
   int abort;
-  float lse2[2][2][BQ / 2];  // [warpgroup][buffer][column]
-  float dsum[2][2][BQ / 2];
+  alignas(16) float lse2[2][BQ];  // [warpgroup][query of its current chunk]
+  alignas(16) float dsum[2][BQ];
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -135,11 +145,91 @@ __device__ __forceinline__ void chunk_range(int nb, int lq, int lk, int win_l, i
   nch = hi1 / BQ - c_lo + 1;
 }
 
+// P^T and dS^T of 16 queries of one key row: the high/low parts of P as 8 + 8
+// packed words, of dS as 8 + 8.  `masked` selects the per-element
+// visibility test (rows whose whole chunk is visible skip it).
+template <typename T, bool kCap>
+__device__ __forceinline__ void p_ds_16(const uint32_t *su, const uint32_t *du, const float *lse2,
+                                        const float *dsum, int i, int qlo, int qhi, bool masked,
+                                        float sl2, float cap_in, float cap_l2, uint32_t *ph,
+                                        uint32_t *pl, uint32_t *dh, uint32_t *dl) {
+#pragma unroll
+  for (int e4 = 0; e4 < 4; ++e4) {
+    const float4 l4 = reinterpret_cast<const float4 *>(lse2)[e4];
+    const float4 d4 = reinterpret_cast<const float4 *>(dsum)[e4];
+    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+#pragma unroll
+    for (int e2 = 0; e2 < 2; ++e2) {
+      float pv[2], dv[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int c = 4 * e4 + 2 * e2 + u;
+        const float s = __uint_as_float(su[c]);
+        float p, dcap = 1.f;
+        if constexpr (kCap) {
+          const float t = tanhf(s * cap_in);
+          p = ex2(fmaf(cap_l2, t, -lv[2 * e2 + u]));
+          dcap = 1.f - t * t;
+        } else {
+          p = ex2(fmaf(s, sl2, -lv[2 * e2 + u]));
+        }
+        if (masked && (i + c < qlo || i + c > qhi)) p = 0.f;
+        pv[u] = p;
+        dv[u] = kCap ? p * (__uint_as_float(du[c]) - dv4[2 * e2 + u]) * dcap
+                     : p * (__uint_as_float(du[c]) - dv4[2 * e2 + u]);
+      }
+      split_hi_lo<T>(pv, ph[2 * e4 + e2], pl[2 * e4 + e2]);
+      split_hi_lo<T>(dv, dh[2 * e4 + e2], dl[2 * e4 + e2]);
+    }
+  }
+}
+
+// One chunk of one softmax thread (key row j; row_t = TMEM base + its lane):
+// P^T high/low into the S^T columns `scol`, dS^T high/low into the two
+// [key][query] arrays at ds_hi / ds_hi + kDS.
+template <typename T, bool kCap>
+__device__ __forceinline__ void chunk_p_ds(uint32_t row_t, uint32_t scol, uint8_t *ds_hi, int j,
+                                           const float *lse2, const float *dsum, int i0, int qlo,
+                                           int qhi, float sl2, float cap_in, float cap_l2) {
+  uint32_t su[BQ], du[BQ];
+  tmem_ld32(row_t + scol, *reinterpret_cast<uint32_t(*)[32]>(su));
+  tmem_ld32(row_t + scol + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
+  tmem_ld32(row_t + scol + 64, *reinterpret_cast<uint32_t(*)[32]>(du));
+  tmem_ld32(row_t + scol + 96, *reinterpret_cast<uint32_t(*)[32]>(du + 32));
+  tmem_wait_ld();
+  const bool masked = i0 < qlo || i0 + BQ - 1 > qhi;
+#pragma unroll
+  for (int hq = 0; hq < 2; ++hq) {
+    uint32_t ph[16], pl[16];
+#pragma unroll
+    for (int hv = 0; hv < 2; ++hv) {
+      const int c0 = 32 * hq + 16 * hv;
+      uint32_t dh[8], dl[8];
+      p_ds_16<T, kCap>(su + c0, du + c0, lse2 + c0, dsum + c0, i0 + c0, qlo, qhi, masked, sl2,
+                       cap_in, cap_l2, ph + 8 * hv, pl + 8 * hv, dh, dl);
+      // dS^T: 16 queries = two 16-byte chunks of the row's 128 bytes
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int chunk = c0 / 8 + cc;
+        const uint32_t off = j * 128 + ((chunk ^ (j & 7)) << 4);
+        *reinterpret_cast<uint4 *>(ds_hi + off) =
+            make_uint4(dh[4 * cc], dh[4 * cc + 1], dh[4 * cc + 2], dh[4 * cc + 3]);
+        *reinterpret_cast<uint4 *>(ds_hi + kDS + off) =
+            make_uint4(dl[4 * cc], dl[4 * cc + 1], dl[4 * cc + 2], dl[4 * cc + 3]);
+      }
+    }
+    // P^T of queries [32 hq, 32 hq + 32): high part at columns 32 hq + [0,16),
+    // low part at 32 hq + [16,32), over S^T values this thread has read
+    tmem_st16(row_t + scol + 32 * hq, ph);
+    tmem_st16(row_t + scol + 32 * hq + 16, pl);
+  }
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
-                  const BwdArgs a, const int n_blocks, int *sem, const int sem_per_head) {
+                  const BwdArgs a, const int n_blocks) {
   const FwdArgs &f = a.f;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
@@ -148,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *k_s = smem;
   uint8_t *v_s = smem + kTileK;
   uint8_t *qd_s = smem + 2 * kTileK;           // [stage][Q | dO]
-  uint8_t *pt_s = qd_s + ST * 2 * kChunk;      // [P high | P low | dS high | dS low], each [key][query]
+  uint8_t *ds_s = qd_s + ST * 2 * kChunk;      // [buffer][dS high | dS low], each [key][query]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // CTA -> (key block, kv head, batch): key blocks fastest, so the CTAs of one
@@ -175,15 +265,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.qd_full[s], 1);
       mbar_init(&sh.qd_empty[s], 1);
     }
-    mbar_init(&sh.sdp_full, 1);
-    mbar_init(&sh.st_free, 256);
-    mbar_init(&sh.pds_full, 256);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&sh.mma_done[s], 1);
+      mbar_init(&sh.sdp_full[s], 1);
+      mbar_init(&sh.pds_full[s], 128);
+      mbar_init(&sh.dq_full[s], 1);
       mbar_init(&sh.dq_free[s], 128);
-      mbar_init(&sh.grp_p[s], 128);
+      mbar_init(&sh.grp[s], 128);
     }
-    mbar_init(&sh.grp_q, 128);
+    mbar_init(&sh.all_done, 1);
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -195,195 +284,179 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
+  const uint32_t row_t = tmem + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's TMEM lanes
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (elect_one() && n_iter > 0) {
-      prefetch_tmap(&tq);
-      prefetch_tmap(&tk);
-      prefetch_tmap(&tv);
-      prefetch_tmap(&tdo);
-      mbar_expect_tx(&sh.kv_full, 2 * kTileK);
-      for (int c = 0; c < D / 64; ++c) {
-        tma_load_3d(k_s + c * BN * 128, &tk, &sh.kv_full, c * 64, kvh, k0 + key0);
-        tma_load_3d(v_s + c * BN * 128, &tv, &sh.kv_full, c * 64, kvh, k0 + key0);
-      }
-      int issued = 0;
-      for (int it = 0; it < n_iter; ++it) {
-        const int st = it % ST;
-        const int h = kvh * g + it / nch;
-        const int row = q0 + (c_lo + it % nch) * BQ;
-        if (!wait_bar(sh, &sh.qd_empty[st], ((it / ST) & 1) ^ 1, f.err)) break;
-        mbar_expect_tx(&sh.qd_full[st], 2 * kChunk);
-        uint8_t *dst = qd_s + st * 2 * kChunk;
+  // launched at 128 registers a thread (16 warps):
+  // 128 * (80 + 80 + 2 * 176) <= 512 * 128
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+    if (warp == 0) {
+      // ---------------------------------------------------------- producer
+      if (elect_one() && n_iter > 0) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+        prefetch_tmap(&tdo);
+        mbar_expect_tx(&sh.kv_full, 2 * kTileK);
         for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(dst + c * BQ * 128, &tq, &sh.qd_full[st], c * 64, h, row);
-          tma_load_3d(dst + kChunk + c * BQ * 128, &tdo, &sh.qd_full[st], c * 64, h, row);
+          tma_load_3d(k_s + c * BN * 128, &tk, &sh.kv_full, c * 64, kvh, k0 + key0);
+          tma_load_3d(v_s + c * BN * 128, &tv, &sh.kv_full, c * 64, kvh, k0 + key0);
         }
-        issued = it + 1;
+        int issued = 0;
+        for (int it = 0; it < n_iter; ++it) {
+          const int st = it % ST;
+          const int h = kvh * g + it / nch;
+          const int row = q0 + (c_lo + it % nch) * BQ;
+          if (!wait_bar(sh, &sh.qd_empty[st], ((it / ST) & 1) ^ 1, f.err)) break;
+          mbar_expect_tx(&sh.qd_full[st], 2 * kChunk);
+          uint8_t *dst = qd_s + st * 2 * kChunk;
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_3d(dst + c * BQ * 128, &tq, &sh.qd_full[st], c * 64, h, row);
+            tma_load_3d(dst + kChunk + c * BQ * 128, &tdo, &sh.qd_full[st], c * 64, h, row);
+          }
+          issued = it + 1;
+        }
+        if (*(volatile int *)&sh.abort) {
+          int *noerr = nullptr;
+          mbar_wait(&sh.kv_full, 0, noerr);
+          for (int it = max(0, issued - ST); it < issued; ++it)
+            mbar_wait(&sh.qd_full[it % ST], (it / ST) & 1, noerr);
+        }
       }
-      if (*(volatile int *)&sh.abort) {
-        int *noerr = nullptr;
-        mbar_wait(&sh.kv_full, 0, noerr);
-        for (int it = max(0, issued - ST); it < issued; ++it)
-          mbar_wait(&sh.qd_full[it % ST], (it / ST) & 1, noerr);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (elect_one() && n_iter > 0) {
-      constexpr int ab = IsBf16<T>::v;
-      constexpr uint32_t id_s = idesc_f16(128, BQ, ab, 0, 0);   // S^T, dP^T
-      constexpr uint32_t id_kv = idesc_f16(128, D, ab, 0, 1);   // dV, dK (B = dO/Q, MN-major)
-      constexpr uint32_t id_q = idesc_f16(128, BQ, ab, 1, 1);   // dQ^T (A = K^T, B = dS^T)
-      const uint32_t k_addr = smem_u32(k_s), v_addr = smem_u32(v_s);
-      const uint32_t qd_addr = smem_u32(qd_s), pt_addr = smem_u32(pt_s);
-      // descriptor bases; every operand below is base + constant offset
-      const uint64_t k_kd = smem_desc(k_addr, 16, 1024), v_kd = smem_desc(v_addr, 16, 1024);
-      const uint64_t k_mn = smem_desc(k_addr, BN * 128, 1024);
-      const uint64_t qd_k = smem_desc(qd_addr, 16, 1024), qd_mn = smem_desc(qd_addr, BQ * 128, 1024);
-      const uint64_t pt_k = smem_desc(pt_addr, 16, 1024), pt_mn = smem_desc(pt_addr, BQ * 128, 1024);
-      auto issue_sdp = [&](int it) -> bool {
-        const int st = it % ST;
-        if (!wait_bar(sh, &sh.qd_full[st], (it / ST) & 1, f.err)) return false;
-        tc_fence_after();
-        const uint32_t q_o = st * 2 * kChunk, do_o = q_o + kChunk;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
-          const uint32_t qo = (kk / 4) * (BQ * 128) + (kk % 4) * 32;
-          mma_ss(tmem + kColS, desc_add(k_kd, ko), desc_add(qd_k, q_o + qo), id_s, kk > 0);
-          mma_ss(tmem + kColDP, desc_add(v_kd, ko), desc_add(qd_k, do_o + qo), id_s, kk > 0);
-        }
-        mma_commit(&sh.sdp_full);
-        return true;
-      };
-      bool ok = wait_bar(sh, &sh.kv_full, 0, f.err) && issue_sdp(0);
-      for (int it = 0; ok && it < n_iter; ++it) {
-        if (it + 1 < n_iter) {
-          if (!wait_bar(sh, &sh.st_free, it & 1, f.err)) break;
-          if (!issue_sdp(it + 1)) break;
-        }
-        const int buf = it & 1, st = it % ST;
-        if (!wait_bar(sh, &sh.pds_full, it & 1, f.err)) break;
-        tc_fence_after();
-        const uint32_t q_o = st * 2 * kChunk, do_o = q_o + kChunk;
-#pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {
-          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          const uint64_t do_d = desc_add(qd_mn, do_o + kk * 16 * 128);
-          const uint64_t q_d = desc_add(qd_mn, q_o + kk * 16 * 128);
-          // dV += (P_high + P_low)^T dO,  dK += (dS_high + dS_low)^T Q
-          mma_ss(tmem + kColDV, desc_add(pt_k, 0 * kPT + kk * 32), do_d, id_kv, acc);
-          mma_ss(tmem + kColDV, desc_add(pt_k, 1 * kPT + kk * 32), do_d, id_kv, 1u);
-          mma_ss(tmem + kColDK, desc_add(pt_k, 2 * kPT + kk * 32), q_d, id_kv, acc);
-          mma_ss(tmem + kColDK, desc_add(pt_k, 3 * kPT + kk * 32), q_d, id_kv, 1u);
-        }
-        mma_commit(&sh.qd_empty[st]);  // Q and dO of this chunk are no longer read
-        if (with_dq) {
-          if (it >= 2 && !wait_bar(sh, &sh.dq_free[buf], ((it >> 1) - 1) & 1, f.err)) break;
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
+      if (elect_one() && n_iter > 0) {
+        constexpr int ab = IsBf16<T>::v;
+        constexpr uint32_t id_s = idesc_f16(128, BQ, ab, 0, 0);   // S^T, dP^T
+        constexpr uint32_t id_kv = idesc_f16(128, D, ab, 0, 1);   // dV, dK (B = dO/Q, MN-major)
+        constexpr uint32_t id_q = idesc_f16(128, BQ, ab, 1, 1);   // dQ^T (A = K^T, B = dS^T)
+        const uint32_t k_addr = smem_u32(k_s), v_addr = smem_u32(v_s);
+        const uint32_t qd_addr = smem_u32(qd_s), ds_addr = smem_u32(ds_s);
+        // descriptor bases; every operand below is base + constant offset
+        const uint64_t k_kd = smem_desc(k_addr, 16, 1024), v_kd = smem_desc(v_addr, 16, 1024);
+        const uint64_t k_mn = smem_desc(k_addr, BN * 128, 1024);
+        const uint64_t qd_k = smem_desc(qd_addr, 16, 1024), qd_mn = smem_desc(qd_addr, BQ * 128, 1024);
+        const uint64_t ds_k = smem_desc(ds_addr, 16, 1024), ds_mn = smem_desc(ds_addr, BQ * 128, 1024);
+        auto issue_sdp = [&](int it) -> bool {
+          const int st = it % ST;
+          if (!wait_bar(sh, &sh.qd_full[st], (it / ST) & 1, f.err)) return false;
           tc_fence_after();
+          const uint32_t buf = tmem + kColBuf + 128 * (it & 1);
+          const uint32_t q_o = st * 2 * kChunk, do_o = q_o + kChunk;
 #pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ss(tmem + kColDQ + buf * BQ, desc_add(k_mn, kk * 16 * 128),
-                   desc_add(pt_mn, 2 * kPT + kk * 16 * 128), id_q, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+            const uint32_t qo = (kk / 4) * (BQ * 128) + (kk % 4) * 32;
+            mma_ss(buf, desc_add(k_kd, ko), desc_add(qd_k, q_o + qo), id_s, kk > 0);
+            mma_ss(buf + 64, desc_add(v_kd, ko), desc_add(qd_k, do_o + qo), id_s, kk > 0);
+          }
+          mma_commit(&sh.sdp_full[it & 1]);
+          return true;
+        };
+        bool ok = wait_bar(sh, &sh.kv_full, 0, f.err) && issue_sdp(0) &&
+                  (n_iter < 2 || issue_sdp(1));
+        // S/dP(0) S/dP(1) | dQ(it) dV(it) dK(it) S/dP(it+2) | ...
+        for (int it = 0; ok && it < n_iter; ++it) {
+          const int bf = it & 1, st = it % ST;
+          const uint32_t par = (it >> 1) & 1;
+          const uint32_t buf = tmem + kColBuf + 128 * bf;
+          const uint32_t dso = bf * 2 * kDS;
+          if (!wait_bar(sh, &sh.pds_full[bf], par, f.err)) break;
+          tc_fence_after();
+          if (with_dq) {
+            // dQ^T = K^T dS^T (high part) into the dP^T columns, already read
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+              mma_ss(buf + 64, desc_add(k_mn, kk * 16 * 128), desc_add(ds_mn, dso + kk * 16 * 128),
+                     id_q, kk > 0);
+            mma_commit(&sh.dq_full[bf]);
+          }
+          const uint32_t q_o = st * 2 * kChunk, do_o = q_o + kChunk;
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk) {
+            const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+            const uint64_t do_d = desc_add(qd_mn, do_o + kk * 16 * 128);
+            const uint64_t q_d = desc_add(qd_mn, q_o + kk * 16 * 128);
+            const uint32_t pc = buf + (kk / 2) * 32 + (kk % 2) * 8;
+            // dV += (P_high + P_low)^T dO,  dK += (dS_high + dS_low)^T Q
+            mma_ts(tmem + kColDV, pc, do_d, id_kv, acc);
+            mma_ts(tmem + kColDV, pc + 16, do_d, id_kv, 1u);
+            mma_ss(tmem + kColDK, desc_add(ds_k, dso + kk * 32), q_d, id_kv, acc);
+            mma_ss(tmem + kColDK, desc_add(ds_k, dso + kDS + kk * 32), q_d, id_kv, 1u);
+          }
+          mma_commit(&sh.qd_empty[st]);  // Q and dO of this chunk are no longer read
+          if (it + 2 < n_iter) {
+            // the dQ^T of this buffer must be out of TMEM before dP^T(it + 2)
+            if (with_dq && !wait_bar(sh, &sh.dq_free[bf], par, f.err)) break;
+            tc_fence_after();
+            if (!issue_sdp(it + 2)) break;
+          }
         }
-        mma_commit(&sh.mma_done[buf]);
+        // completes when every MMA above has; on abort, wait (bounded) so
+        // no MMA is in flight when the TMEM is released
+        mma_commit(&sh.all_done);
+        if (*(volatile int *)&sh.abort) {
+          int *noerr = nullptr;
+          mbar_wait(&sh.all_done, 0, noerr);
+        }
       }
     }
-  } else if (warp < 10) {
+  } else if (warp < 12) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 176;" ::: "memory");
     // ------------------------------------------------------------ P^T, dS^T
-    const int sw = (warp - 2) >> 2;         // which half of the chunk's 64 queries
-    const int tid = threadIdx.x - 64 - 128 * sw;
+    const int w = (warp - 4) >> 2;          // buffer / chunk parity of this warpgroup
+    const int tid = threadIdx.x - 128 * (1 + w);
     const int j = 32 * (warp & 3) + lane;  // TMEM lane = key row of the block
     const int kj = key0 + j;
-    const uint32_t row_t = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
     int qlo, qhi;
     query_range(kj, lq, lk, f.win_l, f.win_r, qlo, qhi);
     if (kj >= lk) qhi = -1;
     const bool cap = f.softcap > 0.f;
     const float sl2 = f.scale * kLog2e, cap_in = cap ? f.scale / f.softcap : 0.f;
+    const float cap_l2 = f.softcap * kLog2e;
+    uint8_t *ds_hi = ds_s + w * 2 * kDS;
+    const uint32_t scol = kColBuf + 128 * w;
     bool ok = true;
-    // thread tid < 32 fetches the LSE of query column 32*sw + tid of a chunk,
-    // 32 <= tid < 64 its D; the fetch for iteration it+1 is issued during it
+    // thread tid < 64 fetches the LSE of query tid of a chunk, 64 <= tid its
+    // D; the fetch for this warpgroup's next chunk is issued during the current
     auto fetch = [&](int it) -> float {
-      if (it >= n_iter || tid >= 64) return 0.f;
+      if (it >= n_iter) return 0.f;
       const int h = kvh * g + it / nch;
-      const int i = (c_lo + it % nch) * BQ + 32 * sw + (tid & 31);
+      const int i = (c_lo + it % nch) * BQ + (tid & 63);
       if (i >= lq) return 0.f;
       const int64_t li = f.seqs.lse_index(b, h, q0, i);
-      return tid < 32 ? f.lse[li] * kLog2e : a.dsum[li];
+      return tid < 64 ? f.lse[li] * kLog2e : a.dsum[li];
     };
-    float next = fetch(0);
-    for (int it = 0; it < n_iter; ++it) {
-      const int buf = it & 1;
-      const int i0 = (c_lo + it % nch) * BQ + 32 * sw;
-      if (tid < 32)
-        sh.lse2[sw][buf][tid] = next;
-      else if (tid < 64)
-        sh.dsum[sw][buf][tid - 32] = next;
-      next = fetch(it + 1);
-      mbar_arrive(&sh.grp_p[sw]);  // this half's LSE and D are in shared memory
-      if (!wait_warp(sh, &sh.grp_p[sw], it & 1, f.err)) { ok = false; break; }
-      if (!wait_warp(sh, &sh.sdp_full, it & 1, f.err)) { ok = false; break; }
+    float next = fetch(w);
+    for (int it = w, n = 0; it < n_iter; it += 2, ++n) {
+      const int par = n & 1;
+      const int i0 = (c_lo + it % nch) * BQ;
+      // every thread of this warpgroup is done with the previous chunk's LSE and D
+      if (n > 0 && !wait_warp(sh, &sh.pds_full[w], par ^ 1, f.err)) { ok = false; break; }
+      if (tid < 64)
+        sh.lse2[w][tid] = next;
+      else
+        sh.dsum[w][tid - 64] = next;
+      next = fetch(it + 2);
+      mbar_arrive(&sh.grp[w]);  // this chunk's LSE and D are in shared memory
+      if (!wait_warp(sh, &sh.grp[w], par, f.err)) { ok = false; break; }
+      // S^T, dP^T of this chunk; the commit behind it also covers the MMAs of
+      // this buffer's previous chunk, so its dS^T arrays are free
+      if (!wait_warp(sh, &sh.sdp_full[w], par, f.err)) { ok = false; break; }
       tc_fence_after();
-      uint32_t su[32], du[32];
-      tmem_ld32(row_t + kColS + 32 * sw, su);
-      tmem_ld32(row_t + kColDP + 32 * sw, du);
-      tmem_wait_ld();
-      tc_fence_before();
-      mbar_arrive(&sh.st_free);
-      // the MMAs of the previous chunk must be done reading the P/dS buffers
-      if (it >= 1 && !wait_warp(sh, &sh.mma_done[(it - 1) & 1], ((it - 1) >> 1) & 1, f.err)) {
-        ok = false;
-        break;
-      }
-      // two halves of 16 columns: compute, split into high and low 16-bit
-      // parts, store (each row is 128 bytes; this warpgroup owns 64 of them)
-#pragma unroll
-      for (int hv = 0; hv < 2; ++hv) {
-        uint32_t w[4][8];  // [P high, P low, dS high, dS low][8 packed pairs]
-#pragma unroll
-        for (int e = 0; e < 16; e += 2) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int u = 0; u < 2; ++u) {
-            const int col = 16 * hv + e + u;
-            const int i = i0 + col;
-            const float s = __uint_as_float(su[col]);
-            float x, dcap = 1.f;
-            if (cap) {
-              const float t = tanhf(s * cap_in);
-              x = f.softcap * t * kLog2e;
-              dcap = 1.f - t * t;
-            } else {
-              x = s * sl2;
-            }
-            const bool vis = i >= qlo && i <= qhi;
-            const float p = vis ? ex2(x - sh.lse2[sw][buf][col]) : 0.f;
-            pv[u] = p;
-            dv[u] = p * (__uint_as_float(du[col]) - sh.dsum[sw][buf][col]) * dcap;
-          }
-          split_hi_lo<T>(pv, w[0][e / 2], w[1][e / 2]);
-          split_hi_lo<T>(dv, w[2][e / 2], w[3][e / 2]);
-        }
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const int chunk = 4 * sw + 2 * hv + cc;  // 16-byte chunk of the 128-byte row
-            const uint32_t off = j * 128 + ((chunk ^ (j & 7)) << 4);
-            *reinterpret_cast<uint4 *>(pt_s + m * kPT + off) =
-                make_uint4(w[m][4 * cc], w[m][4 * cc + 1], w[m][4 * cc + 2], w[m][4 * cc + 3]);
-          }
-        }
-      }
+      if (cap)
+        chunk_p_ds<T, true>(row_t, scol, ds_hi, j, sh.lse2[w], sh.dsum[w], i0,
+                            qlo, qhi, sl2, cap_in, cap_l2);
+      else
+        chunk_p_ds<T, false>(row_t, scol, ds_hi, j, sh.lse2[w], sh.dsum[w], i0,
+                             qlo, qhi, sl2, cap_in, cap_l2);
+      tmem_wait_st();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      mbar_arrive(&sh.pds_full);
+      tc_fence_before();
+      mbar_arrive(&sh.pds_full[w]);
     }
     // dK, dV out of TMEM: each warpgroup writes half of the head-dim columns
-    if (ok && n_iter > 0)
-      ok = wait_warp(sh, &sh.mma_done[(n_iter - 1) & 1], ((n_iter - 1) >> 1) & 1, f.err);
+    if (ok && n_iter > 0) ok = wait_warp(sh, &sh.all_done, 0, f.err);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     // tcgen05.ld is warp-collective: every lane loads, only real keys store
@@ -392,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       T *dvr = static_cast<T *>(a.dv) + off;
       T *dkr = static_cast<T *>(a.dk) + off;
 #pragma unroll 1
-      for (int c = 2 * sw; c < 2 * sw + 2; ++c) {
+      for (int c = 2 * w; c < 2 * w + 2; ++c) {
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           uint32_t u[32];
@@ -404,79 +477,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int e = 0; e < 32; ++e) u[e] = 0u;
           }
           const float sc = which ? f.scale : 1.f;
-          uint32_t w[16];
+          uint32_t o[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            w[e] = Elem<T>::from_f2(__uint_as_float(u[2 * e]) * sc, __uint_as_float(u[2 * e + 1]) * sc);
+            o[e] = Elem<T>::from_f2(__uint_as_float(u[2 * e]) * sc, __uint_as_float(u[2 * e + 1]) * sc);
           if (kj < lk) {
             uint4 *dst = reinterpret_cast<uint4 *>((which ? dkr : dvr) + c * 32);
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-              dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+              dst[e] = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
           }
         }
       }
     }
-  } else if (!with_dq) {
-    // dQ warpgroup idle: the query-stationary kernel computes dQ
   } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
     // ------------------------------------------------------------ dQ
-    const int tid = threadIdx.x - 320;
     const int dl = 32 * (warp & 3) + lane;  // TMEM lane = head-dim column
-    const uint32_t row_t = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
-    uint32_t grp_phase = 0;
-    auto group_sync = [&]() -> bool {
-      mbar_arrive(&sh.grp_q);
-      return wait_warp(sh, &sh.grp_q, (grp_phase++) & 1, f.err);
-    };
-    for (int it = 0; it < n_iter; ++it) {
-      const int buf = it & 1;
+    for (int it = 0; with_dq && it < n_iter; ++it) {
+      const int bf = it & 1;
       const int h = kvh * g + it / nch;
-      const int c = c_lo + it % nch;
-      const int i0 = c * BQ;
-      if (!wait_warp(sh, &sh.mma_done[buf], (it >> 1) & 1, f.err)) break;
+      const int i0 = (c_lo + it % nch) * BQ;
+      if (!wait_warp(sh, &sh.dq_full[bf], (it >> 1) & 1, f.err)) break;
       tc_fence_after();
       uint32_t u[BQ];
-      tmem_ld32(row_t + kColDQ + buf * BQ, *reinterpret_cast<uint32_t(*)[32]>(u));
-      tmem_ld32(row_t + kColDQ + buf * BQ + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+      const uint32_t col = kColBuf + 128 * bf + 64;
+      tmem_ld32(row_t + col, *reinterpret_cast<uint32_t(*)[32]>(u));
+      tmem_ld32(row_t + col + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&sh.dq_free[buf]);
-      int *turn_ctr = nullptr;
-      if (a.deterministic) {
-        // key blocks below this one that also add into chunk c go first
-        turn_ctr = sem + (int64_t)h * sem_per_head + (q0 / BQ + b) + c;
-        if (tid == 0) {
-          int turn = 0;
-          for (int nb2 = 0; nb2 < nb; ++nb2) {
-            int cl, nc;
-            chunk_range(nb2, lq, lk, f.win_l, f.win_r, cl, nc);
-            turn += (c >= cl && c < cl + nc) ? 1 : 0;
-          }
-          const uint64_t t0 = globaltimer();
-          int seen;
-          for (uint32_t spin = 0;; ++spin) {
-            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(turn_ctr) : "memory");
-            if (seen >= turn) break;
-            if ((spin & 63) == 63 && (globaltimer() - t0 > kWaitLimitNs || *(volatile int *)&sh.abort)) {
-              raise_error(f.err, kErrTimeout);
-              *(volatile int *)&sh.abort = 1;
-              break;
-            }
-          }
-        }
-        if (!group_sync()) break;  // thread 0 has seen this key block's turn
-      }
+      mbar_arrive(&sh.dq_free[bf]);
       float *acc = a.dq_acc + ((int64_t)(q0 + i0) * f.hq + h) * D + dl;
       const int rows = min(BQ, lq - i0);
 #pragma unroll
       for (int e = 0; e < BQ; ++e)
         if (e < rows) red_add(acc + (int64_t)e * f.hq * D, __uint_as_float(u[e]));
-      if (a.deterministic) {
-        __threadfence();
-        if (!group_sync()) break;  // every add of this key block is performed
-        if (tid == 0) atomicAdd(turn_ctr, 1);
-      }
     }
   }
   tc_fence_before();
@@ -484,11 +519,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// D_i = rowsum(dO_i * O_i) (fp32, LSE layout); zero the dQ accumulator and
-// the turn counters.  One warp per (row, head).
+// D_i = rowsum(dO_i * O_i) (fp32, LSE layout); zero the dQ accumulator of
+// the atomic mode.  One warp per (row, head).
 template <typename T>
-__global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int *sem, int64_t sem_count,
-                                                       int64_t rows) {
+__global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int64_t rows) {
   const FwdArgs &f = a.f;
   const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -515,8 +549,6 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int *sem, int6
       a.dsum[li] = s;
     }
   }
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  for (int64_t x = t; x < sem_count; x += (int64_t)gridDim.x * blockDim.x) sem[x] = 0;
 }
 
 // dQ = scale * dQ_acc -> dtype.
@@ -532,14 +564,13 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdArgs a, int64_t 
 }
 
 template <typename T>
-cudaError_t bwd_tc(const BwdArgs &a, int *sem, int sem_per_head, int sms, cudaStream_t st) {
+cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
   const FwdArgs &f = a.f;
   const int64_t rows_q = f.seqs.cu_q ? f.seqs.total_q : (int64_t)f.batch * f.seqs.sq;
   const int64_t rows_k = f.seqs.cu_k ? f.seqs.total_k : (int64_t)f.batch * f.seqs.sk;
-  const int64_t sem_count = (int64_t)sem_per_head * f.hq;
   const int prep_blocks = (int)std::min<int64_t>((rows_q * f.hq + 7) / 8, (int64_t)sms * 16);
   if (rows_q > 0) {
-    bwd_prep_kernel<T><<<std::max(prep_blocks, 1), 256, 0, st>>>(a, sem, sem_count, rows_q);
+    bwd_prep_kernel<T><<<std::max(prep_blocks, 1), 256, 0, st>>>(a, rows_q);
     count_launches(1);
   }
   if (rows_k > 0 && rows_q > 0) {
@@ -555,8 +586,7 @@ cudaError_t bwd_tc(const BwdArgs &a, int *sem, int sem_per_head, int sms, cudaSt
     const int n_blocks = (f.seqs.sk + BN - 1) / BN;
     const int64_t grid = (int64_t)n_blocks * f.hkv * f.batch;
     if (grid > INT32_MAX) return cudaErrorInvalidValue;
-    bwd_tc_kernel<T><<<(unsigned)grid, kThreads, kSmem, st>>>(tq, tk, tv, tdo, a, n_blocks, sem,
-                                                              sem_per_head);
+    bwd_tc_kernel<T><<<(unsigned)grid, kThreads, kSmem, st>>>(tq, tk, tv, tdo, a, n_blocks);
     count_launches(1);
   } else if (rows_k > 0) {  // no queries: the key gradients are zero
     const size_t bytes = (size_t)rows_k * f.hkv * D * 2;
@@ -579,11 +609,10 @@ cudaError_t bwd_tc(const BwdArgs &a, int *sem, int sem_per_head, int sms, cudaSt
 
 }  // namespace
 
-cudaError_t launch_bwd_tc(const BwdArgs &a, int *sem, int sem_per_head, int sms,
-                          cudaStream_t st) {
+cudaError_t launch_bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
   if (a.f.d != D) return cudaErrorInvalidValue;
-  return a.f.dtype == ATTN_BF16 ? bwd_tc<__nv_bfloat16>(a, sem, sem_per_head, sms, st)
-                                : bwd_tc<__half>(a, sem, sem_per_head, sms, st);
+  return a.f.dtype == ATTN_BF16 ? bwd_tc<__nv_bfloat16>(a, sms, st)
+                                : bwd_tc<__half>(a, sms, st);
 }
 
 }  // namespace attn

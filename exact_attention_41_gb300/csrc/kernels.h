@@ -60,10 +60,9 @@ void count_launches(int n);
 
 cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t st);
 cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t st);
-// Backward on the tensor cores (d = 128).  sem: turn counters (hq *
-// sem_per_head ints) for the deterministic mode.
-cudaError_t launch_bwd_tc(const BwdArgs &a, int *sem, int sem_per_head, int sms,
-                          cudaStream_t st);
+// Backward on the tensor cores (d = 128): preprocess, key-stationary dK/dV
+// kernel (with atomic dQ unless deterministic), dQ finish.
+cudaError_t launch_bwd_tc(const BwdArgs &a, int sms, cudaStream_t st);
 cudaError_t launch_bwd_simt(const BwdArgs &a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
 
