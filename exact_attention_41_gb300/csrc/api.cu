@@ -64,7 +64,7 @@ attn_status launched(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_E
 // layout) and, unless deterministic, the fp32 dQ accumulator of the
 // key-stationary kernel's atomic adds.
 size_t bwd_ws_bytes(int64_t rows, int hq, int d, int deterministic) {
-  return align256(sizeof(float) * rows * hq) +
+  return align256(sizeof(float2) * rows * hq) +
          (deterministic ? 0 : align256(sizeof(float) * rows * hq * d));
 }
 
@@ -73,8 +73,9 @@ attn_status run_bwd(BwdArgs &a, int64_t rows, void *workspace, const DeviceInfo 
                     cudaStream_t stream) {
   char *ws = static_cast<char *>(workspace);
   const int hq = a.f.hq;
-  a.dsum = reinterpret_cast<float *>(ws);
-  ws += align256(sizeof(float) * rows * hq);
+  a.dsum = reinterpret_cast<float *>(ws);   // one of the two, by path
+  a.lsd = reinterpret_cast<float2 *>(ws);
+  ws += align256(sizeof(float2) * rows * hq);
   a.dq_acc = a.deterministic ? nullptr : reinterpret_cast<float *>(ws);
   if (a.f.d == 128) return launched(launch_bwd_tc(a, di->sms, stream));
   return launched(launch_bwd_simt(a, stream));
@@ -168,7 +169,7 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *ou
   BwdArgs a{FwdArgs{q, k, v, const_cast<void *>(out), const_cast<float *>(lse),
                     Seqs{nullptr, nullptr, sq, sk, 0, 0, hq}, b, hq, hkv, d, dtype, scale,
                     softcap > 0.f ? softcap : 0.f, win_l, win_r, di->err},
-            dout, dq, dk, dv, nullptr, nullptr, deterministic};
+            dout, dq, dk, dv, nullptr, nullptr, nullptr, deterministic};
   return run_bwd(a, (int64_t)b * sq, workspace, di, stream);
 }
 
@@ -236,7 +237,7 @@ attn_status attn_bwd_varlen(const void *q, const void *k, const void *v, const v
                     Seqs{cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, total_q, total_k, hq},
                     batch, hq, hkv, d, dtype, scale, softcap > 0.f ? softcap : 0.f, win_l, win_r,
                     di->err},
-            dout, dq, dk, dv, nullptr, nullptr, deterministic};
+            dout, dq, dk, dv, nullptr, nullptr, nullptr, deterministic};
   return run_bwd(a, total_q, workspace, di, stream);
 }
 

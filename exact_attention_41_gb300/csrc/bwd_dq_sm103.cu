@@ -52,20 +52,7 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 __device__ __forceinline__ bool wait_bar(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_test(a, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t spin = 1;; ++spin) {
-    if (mbar_test(a, parity)) return true;
-    if ((spin & 255) == 0) {
-      if (*(volatile int *)&sh.abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        raise_error(err, kErrTimeout);
-        *(volatile int *)&sh.abort = 1;
-        return false;
-      }
-    }
-  }
+  return mbar_wait_bounded(smem_u32(bar), parity, &sh.abort, err);
 }
 
 __device__ __forceinline__ bool wait_warp(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
@@ -240,8 +227,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     key_range(m0 + t * BM, lq, lk, f.win_l, f.win_r, dummy, hi_tile_min);
     const bool valid = i < lq;
     const int64_t li = f.seqs.lse_index(b, h, q0, valid ? i : 0);
-    const float lse2 = valid ? f.lse[li] * kLog2e : 0.f;
-    const float dsum = valid ? a.dsum[li] : 0.f;
+    const float2 ld = valid ? a.lsd[li] : make_float2(0.f, 0.f);  // (LSE * log2(e), D)
+    const float lse2 = ld.x, dsum = ld.y;
     const bool cap = f.softcap > 0.f;
     const float sl2 = f.scale * kLog2e, cap_in = cap ? f.scale / f.softcap : 0.f;
     bool ok = true;

@@ -10,9 +10,9 @@
 //
 // One CTA owns a block of 128 keys of one (batch, KV head) and loops over the
 // query heads of its GQA group and the 64-row query chunks that can see those
-// keys.  Two chunks are in flight: chunk `it` uses TMEM buffer it % 2 and is
-// handled by softmax warpgroup it % 2, so one chunk's exponentials overlap
-// the other chunk's matrix products.  Roles (16 warps):
+// keys.  Two chunks are in flight: chunk `it` uses TMEM buffer it % 2, so
+// the exponentials of one chunk overlap the matrix products of the previous
+// one.  Roles (16 warps):
 //
 //   warp 0         TMA producer: K and V once, Q and dO chunks into a 3-stage
 //                  ring.
@@ -20,8 +20,8 @@
 //                  into the chunk's buffer; then dQ^T = K^T dS^T into the dP^T
 //                  columns (already read), dV += P^T dO with P^T read from
 //                  TMEM, dK += dS^T Q with dS^T from shared memory.
-//   warps 4-7,     one softmax warpgroup per buffer, one thread per key row:
-//   warps 8-11     P^T and dS^T of the row's 64 queries, each split into a
+//   warps 4-7,     two softmax warpgroups, one thread per (key row, half of
+//   warps 8-11     the chunk's 64 queries): P^T and dS^T, each split into a
 //                  high and a low 16-bit part (so the dV and dK products see
 //                  P and dS to about 16 significant bits); P^T goes back into
 //                  the S^T columns, dS^T into shared memory.  At the end each
@@ -68,11 +68,10 @@ struct Shared {
   uint64_t pds_full[2];  // its P^T (TMEM) and dS^T (shared memory) are written
   uint64_t dq_full[2], dq_free[2];
   uint64_t all_done;     // every MMA of the CTA has completed
-  uint64_t grp[2];       // bounded barrier of each softmax warpgroup
   uint32_t tmem_base;
   int abort;
-  alignas(16) float lse2[2][BQ];  // [warpgroup][query of its current chunk]
-  alignas(16) float dsum[2][BQ];
+  // (LSE * log2(e), D) of each ring stage's 64 queries, copied with the stage
+  alignas(16) float2 lsd[ST][BQ];
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -82,26 +81,18 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 __device__ __forceinline__ bool wait_bar(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_test(a, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t spin = 1;; ++spin) {
-    if (mbar_test(a, parity)) return true;
-    if ((spin & 255) == 0) {
-      if (*(volatile int *)&sh.abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        raise_error(err, kErrTimeout);
-        *(volatile int *)&sh.abort = 1;
-        return false;
-      }
-    }
-  }
+  return mbar_wait_bounded(smem_u32(bar), parity, &sh.abort, err);
 }
 
 // The same wait taken by a whole warp with one answer, so warp-collective
 // tcgen05 loads/stores that follow are never reached by part of a warp.
 __device__ __forceinline__ bool wait_warp(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
-  return __all_sync(0xffffffffu, wait_bar(sh, bar, parity, err));
+  // lane 0 polls (one shared-memory poll per warp, not 32); __syncwarp
+  // orders the other lanes after its wait, __shfl_sync hands them its answer
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(sh, bar, parity, err);
+  __syncwarp();
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
 template <typename T> struct IsBf16 { static constexpr int v = 0; };
@@ -149,15 +140,16 @@ __device__ __forceinline__ void chunk_range(int nb, int lq, int lk, int win_l, i
 // packed words, of dS as 8 + 8.  `masked` selects the per-element
 // visibility test (rows whose whole chunk is visible skip it).
 template <typename T, bool kCap>
-__device__ __forceinline__ void p_ds_16(const uint32_t *su, const uint32_t *du, const float *lse2,
-                                        const float *dsum, int i, int qlo, int qhi, bool masked,
+__device__ __forceinline__ void p_ds_16(const uint32_t *su, const uint32_t *du, const float2 *lsd,
+                                        int i, int qlo, int qhi, bool masked,
                                         float sl2, float cap_in, float cap_l2, uint32_t *ph,
                                         uint32_t *pl, uint32_t *dh, uint32_t *dl) {
 #pragma unroll
   for (int e4 = 0; e4 < 4; ++e4) {
-    const float4 l4 = reinterpret_cast<const float4 *>(lse2)[e4];
-    const float4 d4 = reinterpret_cast<const float4 *>(dsum)[e4];
-    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv4[4] = {d4.x, d4.y, d4.z, d4.w};
+    // (lse, D) of columns 4 e4 .. 4 e4 + 3: two 16-byte loads
+    const float4 a4 = reinterpret_cast<const float4 *>(lsd)[2 * e4];
+    const float4 b4 = reinterpret_cast<const float4 *>(lsd)[2 * e4 + 1];
+    const float lv[4] = {a4.x, a4.z, b4.x, b4.z}, dv4[4] = {a4.y, a4.w, b4.y, b4.w};
 #pragma unroll
     for (int e2 = 0; e2 < 2; ++e2) {
       float pv[2], dv[2];
@@ -184,45 +176,40 @@ __device__ __forceinline__ void p_ds_16(const uint32_t *su, const uint32_t *du, 
   }
 }
 
-// One chunk of one softmax thread (key row j; row_t = TMEM base + its lane):
-// P^T high/low into the S^T columns `scol`, dS^T high/low into the two
-// [key][query] arrays at ds_hi / ds_hi + kDS.
+// Half a chunk of one softmax thread (key row j; row_t = TMEM base + its
+// lane): the 32 queries [32 hq, 32 hq + 32) of the chunk in buffer `buf`.
+// P^T high/low go back over the S^T columns just read (high at 32 hq +
+// [0,16), low at 32 hq + [16,32)); dS^T high/low into the two [key][query]
+// arrays at ds_hi / ds_hi + kDS.
 template <typename T, bool kCap>
-__device__ __forceinline__ void chunk_p_ds(uint32_t row_t, uint32_t scol, uint8_t *ds_hi, int j,
-                                           const float *lse2, const float *dsum, int i0, int qlo,
-                                           int qhi, float sl2, float cap_in, float cap_l2) {
-  uint32_t su[BQ], du[BQ];
-  tmem_ld32(row_t + scol, *reinterpret_cast<uint32_t(*)[32]>(su));
-  tmem_ld32(row_t + scol + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
-  tmem_ld32(row_t + scol + 64, *reinterpret_cast<uint32_t(*)[32]>(du));
-  tmem_ld32(row_t + scol + 96, *reinterpret_cast<uint32_t(*)[32]>(du + 32));
+__device__ __forceinline__ void half_p_ds(uint32_t row_t, uint32_t buf, int hq, uint8_t *ds_hi,
+                                          int j, const float2 *lsd, int i0, int qlo, int qhi,
+                                          float sl2, float cap_in, float cap_l2) {
+  uint32_t su[32], du[32];
+  tmem_ld32(row_t + buf + 32 * hq, su);
+  tmem_ld32(row_t + buf + 64 + 32 * hq, du);
   tmem_wait_ld();
-  const bool masked = i0 < qlo || i0 + BQ - 1 > qhi;
+  const bool masked = i0 < qlo || i0 + 31 > qhi;
+  uint32_t ph[16], pl[16];
 #pragma unroll
-  for (int hq = 0; hq < 2; ++hq) {
-    uint32_t ph[16], pl[16];
+  for (int hv = 0; hv < 2; ++hv) {
+    const int c0 = 16 * hv;
+    uint32_t dh[8], dl[8];
+    p_ds_16<T, kCap>(su + c0, du + c0, lsd + c0, i0 + c0, qlo, qhi, masked, sl2, cap_in, cap_l2,
+                     ph + 8 * hv, pl + 8 * hv, dh, dl);
+    // dS^T: 16 queries = two 16-byte chunks of the row's 128 bytes
 #pragma unroll
-    for (int hv = 0; hv < 2; ++hv) {
-      const int c0 = 32 * hq + 16 * hv;
-      uint32_t dh[8], dl[8];
-      p_ds_16<T, kCap>(su + c0, du + c0, lse2 + c0, dsum + c0, i0 + c0, qlo, qhi, masked, sl2,
-                       cap_in, cap_l2, ph + 8 * hv, pl + 8 * hv, dh, dl);
-      // dS^T: 16 queries = two 16-byte chunks of the row's 128 bytes
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int chunk = c0 / 8 + cc;
-        const uint32_t off = j * 128 + ((chunk ^ (j & 7)) << 4);
-        *reinterpret_cast<uint4 *>(ds_hi + off) =
-            make_uint4(dh[4 * cc], dh[4 * cc + 1], dh[4 * cc + 2], dh[4 * cc + 3]);
-        *reinterpret_cast<uint4 *>(ds_hi + kDS + off) =
-            make_uint4(dl[4 * cc], dl[4 * cc + 1], dl[4 * cc + 2], dl[4 * cc + 3]);
-      }
+    for (int cc = 0; cc < 2; ++cc) {
+      const int chunk = 4 * hq + 2 * hv + cc;
+      const uint32_t off = j * 128 + ((chunk ^ (j & 7)) << 4);
+      *reinterpret_cast<uint4 *>(ds_hi + off) =
+          make_uint4(dh[4 * cc], dh[4 * cc + 1], dh[4 * cc + 2], dh[4 * cc + 3]);
+      *reinterpret_cast<uint4 *>(ds_hi + kDS + off) =
+          make_uint4(dl[4 * cc], dl[4 * cc + 1], dl[4 * cc + 2], dl[4 * cc + 3]);
     }
-    // P^T of queries [32 hq, 32 hq + 32): high part at columns 32 hq + [0,16),
-    // low part at 32 hq + [16,32), over S^T values this thread has read
-    tmem_st16(row_t + scol + 32 * hq, ph);
-    tmem_st16(row_t + scol + 32 * hq + 16, pl);
   }
+  tmem_st16(row_t + buf + 32 * hq, ph);
+  tmem_st16(row_t + buf + 32 * hq + 16, pl);
 }
 
 template <typename T>
@@ -267,10 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&sh.sdp_full[s], 1);
-      mbar_init(&sh.pds_full[s], 128);
+      mbar_init(&sh.pds_full[s], 8);   // warps
       mbar_init(&sh.dq_full[s], 1);
-      mbar_init(&sh.dq_free[s], 128);
-      mbar_init(&sh.grp[s], 128);
+      mbar_init(&sh.dq_free[s], 4);
     }
     mbar_init(&sh.all_done, 1);
     sh.abort = 0;
@@ -287,36 +273,53 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t row_t = tmem + ((uint32_t)(32 * (warp & 3)) << 16);  // this warp's TMEM lanes
 
   // launched at 128 registers a thread (16 warps):
-  // 128 * (80 + 80 + 2 * 176) <= 512 * 128
+  // 128 * (104 + 104 + 2 * 152) <= 512 * 128
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
     if (warp == 0) {
       // ---------------------------------------------------------- producer
-      if (elect_one() && n_iter > 0) {
-        prefetch_tmap(&tq);
-        prefetch_tmap(&tk);
-        prefetch_tmap(&tv);
-        prefetch_tmap(&tdo);
-        mbar_expect_tx(&sh.kv_full, 2 * kTileK);
-        for (int c = 0; c < D / 64; ++c) {
-          tma_load_3d(k_s + c * BN * 128, &tk, &sh.kv_full, c * 64, kvh, k0 + key0);
-          tma_load_3d(v_s + c * BN * 128, &tv, &sh.kv_full, c * 64, kvh, k0 + key0);
+      // the whole warp copies (LSE * log2(e), D) of each chunk's queries
+      // into the stage with cp.async (zeros past the sequence end); lane 0
+      // issues the TMA loads.  Both complete the stage's qd_full phase.
+      if (n_iter > 0) {
+        if (lane == 0) {
+          prefetch_tmap(&tq);
+          prefetch_tmap(&tk);
+          prefetch_tmap(&tv);
+          prefetch_tmap(&tdo);
+          mbar_expect_tx(&sh.kv_full, 2 * kTileK);
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_3d(k_s + c * BN * 128, &tk, &sh.kv_full, c * 64, kvh, k0 + key0);
+            tma_load_3d(v_s + c * BN * 128, &tv, &sh.kv_full, c * 64, kvh, k0 + key0);
+          }
         }
         int issued = 0;
         for (int it = 0; it < n_iter; ++it) {
           const int st = it % ST;
           const int h = kvh * g + it / nch;
-          const int row = q0 + (c_lo + it % nch) * BQ;
-          if (!wait_bar(sh, &sh.qd_empty[st], ((it / ST) & 1) ^ 1, f.err)) break;
-          mbar_expect_tx(&sh.qd_full[st], 2 * kChunk);
-          uint8_t *dst = qd_s + st * 2 * kChunk;
-          for (int c = 0; c < D / 64; ++c) {
-            tma_load_3d(dst + c * BQ * 128, &tq, &sh.qd_full[st], c * 64, h, row);
-            tma_load_3d(dst + kChunk + c * BQ * 128, &tdo, &sh.qd_full[st], c * 64, h, row);
+          const int i0 = (c_lo + it % nch) * BQ;
+          if (!wait_warp(sh, &sh.qd_empty[st], ((it / ST) & 1) ^ 1, f.err)) break;
+#pragma unroll
+          for (int r = lane; r < BQ; r += 32) {
+            const int i = i0 + r;
+            const bool in = i < lq;
+            cp_async_8(&sh.lsd[st][r], a.lsd + f.seqs.lse_index(b, h, q0, in ? i : 0), in ? 8u : 0u);
+          }
+          cp_async_mbar_arrive(&sh.qd_full[st]);
+          __syncwarp();
+          if (lane == 0) {
+            mbar_expect_tx(&sh.qd_full[st], 2 * kChunk);
+            uint8_t *dst = qd_s + st * 2 * kChunk;
+            for (int c = 0; c < D / 64; ++c) {
+              tma_load_3d(dst + c * BQ * 128, &tq, &sh.qd_full[st], c * 64, h, q0 + i0);
+              tma_load_3d(dst + kChunk + c * BQ * 128, &tdo, &sh.qd_full[st], c * 64, h, q0 + i0);
+            }
           }
           issued = it + 1;
         }
-        if (*(volatile int *)&sh.abort) {
+        cp_async_wait_all();
+        if (lane == 0 && *(volatile int *)&sh.abort) {
+          // let this CTA's copies in flight land before the CTA exits
           int *noerr = nullptr;
           mbar_wait(&sh.kv_full, 0, noerr);
           for (int it = max(0, issued - ST); it < issued; ++it)
@@ -402,10 +405,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else if (warp < 12) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 176;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 152;" ::: "memory");
     // ------------------------------------------------------------ P^T, dS^T
-    const int w = (warp - 4) >> 2;          // buffer / chunk parity of this warpgroup
-    const int tid = threadIdx.x - 128 * (1 + w);
+    const int w = (warp - 4) >> 2;          // which half of every chunk's 64 queries
     const int j = 32 * (warp & 3) + lane;  // TMEM lane = key row of the block
     const int kj = key0 + j;
     int qlo, qhi;
@@ -414,46 +416,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool cap = f.softcap > 0.f;
     const float sl2 = f.scale * kLog2e, cap_in = cap ? f.scale / f.softcap : 0.f;
     const float cap_l2 = f.softcap * kLog2e;
-    uint8_t *ds_hi = ds_s + w * 2 * kDS;
-    const uint32_t scol = kColBuf + 128 * w;
     bool ok = true;
-    // thread tid < 64 fetches the LSE of query tid of a chunk, 64 <= tid its
-    // D; the fetch for this warpgroup's next chunk is issued during the current
-    auto fetch = [&](int it) -> float {
-      if (it >= n_iter) return 0.f;
-      const int h = kvh * g + it / nch;
-      const int i = (c_lo + it % nch) * BQ + (tid & 63);
-      if (i >= lq) return 0.f;
-      const int64_t li = f.seqs.lse_index(b, h, q0, i);
-      return tid < 64 ? f.lse[li] * kLog2e : a.dsum[li];
-    };
-    float next = fetch(w);
-    for (int it = w, n = 0; it < n_iter; it += 2, ++n) {
-      const int par = n & 1;
-      const int i0 = (c_lo + it % nch) * BQ;
-      // every thread of this warpgroup is done with the previous chunk's LSE and D
-      if (n > 0 && !wait_warp(sh, &sh.pds_full[w], par ^ 1, f.err)) { ok = false; break; }
-      if (tid < 64)
-        sh.lse2[w][tid] = next;
-      else
-        sh.dsum[w][tid - 64] = next;
-      next = fetch(it + 2);
-      mbar_arrive(&sh.grp[w]);  // this chunk's LSE and D are in shared memory
-      if (!wait_warp(sh, &sh.grp[w], par, f.err)) { ok = false; break; }
+    for (int it = 0; it < n_iter; ++it) {
+      const int bf = it & 1, st = it % ST;
+      const uint32_t par = (it >> 1) & 1;
+      const int i0 = (c_lo + it % nch) * BQ + 32 * w;
       // S^T, dP^T of this chunk; the commit behind it also covers the MMAs of
-      // this buffer's previous chunk, so its dS^T arrays are free
-      if (!wait_warp(sh, &sh.sdp_full[w], par, f.err)) { ok = false; break; }
+      // this buffer's previous chunk, so its dS^T arrays are free.  The
+      // stage's (LSE, D) copies landed before its S^T was computed; the wait
+      // on qd_full (already complete) makes them visible to this warp.
+      if (!wait_warp(sh, &sh.sdp_full[bf], par, f.err) ||
+          !wait_warp(sh, &sh.qd_full[st], (it / ST) & 1, f.err)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
+      uint8_t *ds_hi = ds_s + bf * 2 * kDS;
+      const uint32_t buf = kColBuf + 128 * bf;
+      const float2 *lsd = sh.lsd[st] + 32 * w;
       if (cap)
-        chunk_p_ds<T, true>(row_t, scol, ds_hi, j, sh.lse2[w], sh.dsum[w], i0,
-                            qlo, qhi, sl2, cap_in, cap_l2);
+        half_p_ds<T, true>(row_t, buf, w, ds_hi, j, lsd, i0, qlo, qhi, sl2, cap_in, cap_l2);
       else
-        chunk_p_ds<T, false>(row_t, scol, ds_hi, j, sh.lse2[w], sh.dsum[w], i0,
-                             qlo, qhi, sl2, cap_in, cap_l2);
+        half_p_ds<T, false>(row_t, buf, w, ds_hi, j, lsd, i0, qlo, qhi, sl2, cap_in, cap_l2);
       tmem_wait_st();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
-      mbar_arrive(&sh.pds_full[w]);
+      mbar_arrive_warp(&sh.pds_full[bf]);
     }
     // dK, dV out of TMEM: each warpgroup writes half of the head-dim columns
     if (ok && n_iter > 0) ok = wait_warp(sh, &sh.all_done, 0, f.err);
@@ -491,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
     // ------------------------------------------------------------ dQ
     const int dl = 32 * (warp & 3) + lane;  // TMEM lane = head-dim column
     for (int it = 0; with_dq && it < n_iter; ++it) {
@@ -506,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(row_t + col + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive(&sh.dq_free[bf]);
+      mbar_arrive_warp(&sh.dq_free[bf]);
       float *acc = a.dq_acc + ((int64_t)(q0 + i0) * f.hq + h) * D + dl;
       const int rows = min(BQ, lq - i0);
 #pragma unroll
@@ -519,8 +507,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-// D_i = rowsum(dO_i * O_i) (fp32, LSE layout); zero the dQ accumulator of
-// the atomic mode.  One warp per (row, head).
+// (LSE_i * log2(e), D_i = rowsum(dO_i * O_i)) per row (fp32, LSE layout);
+// zero the dQ accumulator of the atomic mode.  One warp per (row, head).
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int64_t rows) {
   const FwdArgs &f = a.f;
@@ -546,7 +534,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int64_t rows) 
         const int64_t bb = row / f.seqs.sq, i = row % f.seqs.sq;
         li = (bb * f.hq + h) * f.seqs.sq + i;
       }
-      a.dsum[li] = s;
+      a.lsd[li] = make_float2(f.lse[li] * kLog2e, s);
     }
   }
 }

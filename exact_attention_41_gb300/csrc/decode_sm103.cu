@@ -68,20 +68,7 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 __device__ __forceinline__ bool wait_bar(DecShared &sh, uint64_t *bar, uint32_t parity, int *err) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_test(a, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t spin = 1;; ++spin) {
-    if (mbar_test(a, parity)) return true;
-    if ((spin & 255) == 0) {
-      if (*(volatile int *)&sh.abort) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
-        raise_error(err, kErrTimeout);
-        *(volatile int *)&sh.abort = 1;
-        return false;
-      }
-    }
-  }
+  return mbar_wait_bounded(smem_u32(bar), parity, &sh.abort, err);
 }
 
 // The same wait taken by a whole warp with one answer, so warp-collective

@@ -23,7 +23,8 @@ struct BwdArgs {
   FwdArgs f;             // f.o / f.lse are the forward's outputs (read only)
   const void *dout;
   void *dq, *dk, *dv;
-  float *dsum;           // workspace: D_i = rowsum(dO * O), LSE layout
+  float *dsum;           // workspace: D_i = rowsum(dO * O), LSE layout (CUDA-core path)
+  float2 *lsd;           // workspace: (LSE_i * log2(e), D_i), LSE layout (tensor-core path)
   float *dq_acc;         // workspace: fp32 dQ accumulator (atomic mode)
   int deterministic;
 };

@@ -51,6 +51,15 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
                : "memory");
 }
 
+// One arrival for a whole warp (barrier counts are then in warps).
+// __syncwarp orders every lane's earlier accesses (TMEM ones after a
+// tcgen05.fence::before_thread_sync) before lane 0's release-arrive; 32
+// arrivals on one mbarrier word would be serialised.
+__device__ __forceinline__ void mbar_arrive_warp(uint64_t *bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
                    smem_u32(bar)),
@@ -69,19 +78,51 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits until the phase with the given parity has completed.  Returns false
-// (and raises kErrTimeout) if that takes longer than kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
-  const uint32_t a = smem_u32(bar);
-  if (mbar_test(a, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t spin = 1;; ++spin) {
+// Waits until the phase with the given parity has completed.  Gives up
+// (returns false) when the shared flag `*abort` is set by another role, or
+// after kWaitLimitNs of wall clock, raising kErrTimeout and setting *abort.
+// The wall clock is read only once every 256 failed tests: a %globaltimer
+// read costs far more than an mbarrier test, and most waits end before it.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t a, uint32_t parity, int *abort,
+                                                  int *err) {
+  uint64_t t0 = 0;
+  for (uint32_t spin = 0;; ++spin) {
     if (mbar_test(a, parity)) return true;
-    if ((spin & 255) == 0 && globaltimer() - t0 > kWaitLimitNs) {
-      raise_error(err, kErrTimeout);
-      return false;
+    if ((spin & 255) == 255) {
+      if (abort && *(volatile int *)abort) return false;
+      const uint64_t now = globaltimer();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitNs) {
+        raise_error(err, kErrTimeout);
+        if (abort) *(volatile int *)abort = 1;
+        return false;
+      }
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
+  return mbar_wait_bounded(smem_u32(bar), parity, nullptr, err);
+}
+
+// ------------------------------------------------------------------ cp.async
+
+// 8-byte global -> shared copy; src_bytes = 0 writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async_8(void *dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+
+// The mbarrier's current phase also waits for this thread's cp.async copies
+// issued so far (the pending count is raised now and lowered when they land).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ TMA
