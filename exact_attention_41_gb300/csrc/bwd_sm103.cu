@@ -340,25 +340,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t k_mn = smem_desc(k_addr, BN * 128, 1024);
         const uint64_t qd_k = smem_desc(qd_addr, 16, 1024), qd_mn = smem_desc(qd_addr, BQ * 128, 1024);
         const uint64_t ds_k = smem_desc(ds_addr, 16, 1024), ds_mn = smem_desc(ds_addr, BQ * 128, 1024);
-        auto issue_sdp = [&](int it) -> bool {
+        // S^T = K Q^T (which = 0) or dP^T = V dO^T (which = 1) of chunk `it`
+        // into its buffer; the Q/dO stage must have landed
+        auto issue_s_or_dp = [&](int it, int which) {
           const int st = it % ST;
-          if (!wait_bar(sh, &sh.qd_full[st], (it / ST) & 1, f.err)) return false;
-          tc_fence_after();
-          const uint32_t buf = tmem + kColBuf + 128 * (it & 1);
-          const uint32_t q_o = st * 2 * kChunk, do_o = q_o + kChunk;
+          const uint32_t buf = tmem + kColBuf + 128 * (it & 1) + 64 * which;
+          const uint64_t a_d = which ? v_kd : k_kd;
+          const uint32_t b_o = st * 2 * kChunk + which * kChunk;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ko = (kk / 4) * (BN * 128) + (kk % 4) * 32;
             const uint32_t qo = (kk / 4) * (BQ * 128) + (kk % 4) * 32;
-            mma_ss(buf, desc_add(k_kd, ko), desc_add(qd_k, q_o + qo), id_s, kk > 0);
-            mma_ss(buf + 64, desc_add(v_kd, ko), desc_add(qd_k, do_o + qo), id_s, kk > 0);
+            mma_ss(buf, desc_add(a_d, ko), desc_add(qd_k, b_o + qo), id_s, kk > 0);
           }
-          mma_commit(&sh.sdp_full[it & 1]);
-          return true;
         };
-        bool ok = wait_bar(sh, &sh.kv_full, 0, f.err) && issue_sdp(0) &&
-                  (n_iter < 2 || issue_sdp(1));
-        // S/dP(0) S/dP(1) | dQ(it) dV(it) dK(it) S/dP(it+2) | ...
+        auto stage_ready = [&](int it) -> bool {
+          const bool r = wait_bar(sh, &sh.qd_full[it % ST], (it / ST) & 1, f.err);
+          tc_fence_after();
+          return r;
+        };
+        bool ok = wait_bar(sh, &sh.kv_full, 0, f.err);
+        for (int it = 0; ok && it < min(2, n_iter); ++it) {
+          if (!(ok = stage_ready(it))) break;
+          issue_s_or_dp(it, 0);
+          issue_s_or_dp(it, 1);
+          mma_commit(&sh.sdp_full[it]);
+        }
+        // S/dP(0) S/dP(1) | dQ(it) dV(it) S(it+2) dK(it) dP(it+2) | ...
+        // S(it+2) needs only dV(it) to have read P^T(it) (issue order);
+        // dP(it+2) waits until dQ^T(it) has left the dP^T columns.
         for (int it = 0; ok && it < n_iter; ++it) {
           const int bf = it & 1, st = it % ST;
           const uint32_t par = (it >> 1) & 1;
@@ -377,22 +387,32 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t q_o = st * 2 * kChunk, do_o = q_o + kChunk;
 #pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk) {
+            // dV += (P_high + P_low)^T dO
             const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
             const uint64_t do_d = desc_add(qd_mn, do_o + kk * 16 * 128);
-            const uint64_t q_d = desc_add(qd_mn, q_o + kk * 16 * 128);
             const uint32_t pc = buf + (kk / 2) * 32 + (kk % 2) * 8;
-            // dV += (P_high + P_low)^T dO,  dK += (dS_high + dS_low)^T Q
             mma_ts(tmem + kColDV, pc, do_d, id_kv, acc);
             mma_ts(tmem + kColDV, pc + 16, do_d, id_kv, 1u);
+          }
+          const bool next = it + 2 < n_iter;
+          if (next) {
+            if (!stage_ready(it + 2)) break;
+            issue_s_or_dp(it + 2, 0);
+          }
+#pragma unroll
+          for (int kk = 0; kk < BQ / 16; ++kk) {
+            // dK += (dS_high + dS_low)^T Q
+            const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+            const uint64_t q_d = desc_add(qd_mn, q_o + kk * 16 * 128);
             mma_ss(tmem + kColDK, desc_add(ds_k, dso + kk * 32), q_d, id_kv, acc);
             mma_ss(tmem + kColDK, desc_add(ds_k, dso + kDS + kk * 32), q_d, id_kv, 1u);
           }
           mma_commit(&sh.qd_empty[st]);  // Q and dO of this chunk are no longer read
-          if (it + 2 < n_iter) {
-            // the dQ^T of this buffer must be out of TMEM before dP^T(it + 2)
+          if (next) {
             if (with_dq && !wait_bar(sh, &sh.dq_free[bf], par, f.err)) break;
             tc_fence_after();
-            if (!issue_sdp(it + 2)) break;
+            issue_s_or_dp(it + 2, 1);
+            mma_commit(&sh.sdp_full[bf]);
           }
         }
         // completes when every MMA above has; on abort, wait (bounded) so
