@@ -514,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld32(row_t + col + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
       tmem_wait_ld();
       tc_fence_before();
-      mbar_arrive_warp(&sh.dq_free[bf]);
+      mbar_arrive_relaxed_warp(&sh.dq_free[bf]);  // not behind the previous chunk's adds
       float *acc = a.dq_acc + ((int64_t)(q0 + i0) * f.hq + h) * D + dl;
       const int rows = min(BQ, lq - i0);
 #pragma unroll

@@ -60,6 +60,18 @@ __device__ __forceinline__ void mbar_arrive_warp(uint64_t *bar) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
+// A warp's single relaxed arrival: for a barrier that only announces that
+// this warp's TMEM reads are complete (tcgen05.wait::ld has returned and
+// tcgen05.fence::before_thread_sync was issued).  A release arrival would
+// first wait for the warp's earlier global writes (e.g. reductions still in
+// flight), which the waiting side does not need.
+__device__ __forceinline__ void mbar_arrive_relaxed_warp(uint64_t *bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0)
+    asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
                    smem_u32(bar)),
