@@ -88,8 +88,11 @@ int resolve_splits(int b, int hkv, int max_seqlen_k, int num_splits, int sms) {
   // fewer units than SMs -> split until near the SM count; long caches ->
   // split so each piece streams a bounded key range.
   const int units = max(1, b * hkv);
-  if (units >= sms && max_seqlen_k <= 2048) return 1;
-  int s = (max_seqlen_k + 2047) / 2048;
+  // A piece of 8192 keys (64 tiles) amortises a CTA's start and epilogue;
+  // on the paged decode workload (b=64, hkv=8, caches up to 32K) 4-5 splits
+  // stream at ~6 TB/s and 17 splits of 2048 keys at 5.2 TB/s.
+  if (units >= sms && max_seqlen_k <= 8192) return 1;
+  int s = (max_seqlen_k + 8191) / 8192;
   s = max(s, (sms + units - 1) / units);
   return max(1, min(min(s, 64), max_useful));
 }
@@ -301,6 +304,32 @@ attn_status attn_fwd_kvcache(const void *q, void *k_cache, void *v_cache, const 
                           : nullptr,
                di->err};
   return launched(launch_decode(a, stream));
+}
+
+attn_status attn_fwd_probs(const void *q, const void *k, const float *lse, float *p, int dtype,
+                           int b, int sq, int sk, int hq, int hkv, int d, float scale,
+                           int causal, int win_l, int win_r, float softcap,
+                           attn_stream_t stream) {
+  attn_status st = check_common(dtype, hq, hkv, d, scale, win_l, win_r, causal, softcap);
+  if (st != ATTN_OK) return st;
+  if (b < 0 || sq < 0 || sk < 0) return ATTN_ERR_INVALID;
+  if (b == 0 || sq == 0 || sk == 0) return ATTN_OK;
+  if (!q || !k || !lse || !p) return ATTN_ERR_INVALID;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(lse) || !aligned16(p)) return ATTN_ERR_INVALID;
+  if ((int64_t)b * hq > 65535 || sq > 65535) return ATTN_ERR_UNSUPPORTED;
+  const DeviceInfo *di = device_info();
+  if (!di) return ATTN_ERR_CUDA;
+  FwdArgs a{q, k, nullptr, nullptr, const_cast<float *>(lse),
+            Seqs{nullptr, nullptr, sq, sk, 0, 0, hq}, b, hq, hkv, d, dtype, scale,
+            softcap > 0.f ? softcap : 0.f, win_l, win_r, di->err};
+  return launched(launch_probs(a, p, stream));
+}
+
+attn_status attn_kvcache_advance(int32_t *cache_seqlens, int b, int s_new, attn_stream_t stream) {
+  if (b < 0 || s_new < 0) return ATTN_ERR_INVALID;
+  if (b == 0) return ATTN_OK;
+  if (!cache_seqlens || (reinterpret_cast<uintptr_t>(cache_seqlens) & 3)) return ATTN_ERR_INVALID;
+  return launched(launch_kvcache_advance(cache_seqlens, b, s_new, stream));
 }
 
 unsigned long long attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -321,8 +321,7 @@ cudaError_t bwd_dq(const BwdArgs &a, cudaStream_t st) {
       !make_map_3d(&tk, f.k, f.dtype, rows_k, f.hkv, D, BN) ||
       !make_map_3d(&tv, f.v, f.dtype, rows_k, f.hkv, D, BN))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(bwd_dq_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmem);
+  cudaError_t e = set_smem_once<bwd_dq_kernel<T>>(kSmem);
   if (e != cudaSuccess) return e;
   const int m_blocks = (f.seqs.sq + BM * NT - 1) / (BM * NT);
   const int64_t grid = (int64_t)m_blocks * f.hq * f.batch;

@@ -87,12 +87,7 @@ __device__ __forceinline__ bool wait_bar(Shared &sh, uint64_t *bar, uint32_t par
 // The same wait taken by a whole warp with one answer, so warp-collective
 // tcgen05 loads/stores that follow are never reached by part of a warp.
 __device__ __forceinline__ bool wait_warp(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
-  // lane 0 polls (one shared-memory poll per warp, not 32); __syncwarp
-  // orders the other lanes after its wait, __shfl_sync hands them its answer
-  bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(sh, bar, parity, err);
-  __syncwarp();
-  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  return __all_sync(0xffffffffu, wait_bar(sh, bar, parity, err));
 }
 
 template <typename T> struct IsBf16 { static constexpr int v = 0; };
@@ -588,8 +583,7 @@ cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
         !make_map_3d(&tk, f.k, f.dtype, rows_k, f.hkv, D, BN) ||
         !make_map_3d(&tv, f.v, f.dtype, rows_k, f.hkv, D, BN))
       return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(bwd_tc_kernel<T>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t e = set_smem_once<bwd_tc_kernel<T>>(kSmem);
     if (e != cudaSuccess) return e;
     const int n_blocks = (f.seqs.sk + BN - 1) / BN;
     const int64_t grid = (int64_t)n_blocks * f.hkv * f.batch;

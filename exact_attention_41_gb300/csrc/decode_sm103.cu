@@ -448,8 +448,7 @@ cudaError_t decode_tc(const DecodeArgs &a, cudaStream_t st) {
   if (!make_map_3d(&tk, a.k_cache, a.dtype, pool_rows, a.hkv, D, BK) ||
       !make_map_3d(&tv, a.v_cache, a.dtype, pool_rows, a.hkv, D, BK))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(decode_tc_kernel<T, RP>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  cudaError_t e = set_smem_once<decode_tc_kernel<T, RP>>(C::kSmem);
   if (e != cudaSuccess) return e;
   const int64_t grid = (int64_t)a.num_splits * a.hkv * a.b;
   if (grid > INT32_MAX) return cudaErrorInvalidValue;

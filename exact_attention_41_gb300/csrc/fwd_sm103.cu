@@ -468,8 +468,7 @@ cudaError_t fwd_tc(const FwdArgs &a, cudaStream_t st) {
       !make_map_3d(&tk, a.k, a.dtype, rows_k, a.hkv, D, BN) ||
       !make_map_3d(&tv, a.v, a.dtype, rows_k, a.hkv, D, BN))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(fwd_tc_kernel<T, D, BN, NT>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  cudaError_t e = set_smem_once<fwd_tc_kernel<T, D, BN, NT>>(C::kSmem);
   if (e != cudaSuccess) return e;
   const int m_blocks = (a.seqs.sq + kBM * NT - 1) / (kBM * NT);
   const int64_t grid = (int64_t)m_blocks * a.hq * a.batch;

@@ -3,6 +3,8 @@
 
 #include <cudaTypedefs.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace attn {
@@ -59,6 +61,22 @@ cudaError_t launch_decode_tc(const DecodeArgs &a, cudaStream_t st);
 // Adds n to the library's launch counter (attn_launch_count).
 void count_launches(int n);
 
+// Raises `Kernel`'s dynamic shared memory limit to `bytes`, once per device:
+// later calls (including ones made during CUDA graph capture) only read a
+// flag.
+template <auto Kernel>
+cudaError_t set_smem_once(int bytes) {
+  static std::atomic<unsigned long long> done{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (done.load(std::memory_order_acquire) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t st);
 cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t st);
 // Backward on the tensor cores (d = 128): preprocess, key-stationary dK/dV
@@ -66,5 +84,9 @@ cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t st);
 cudaError_t launch_bwd_tc(const BwdArgs &a, int sms, cudaStream_t st);
 cudaError_t launch_bwd_simt(const BwdArgs &a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
+// Debug probability matrix p (b, hq, sq, sk) fp32 from q, k and a.lse.
+cudaError_t launch_probs(const FwdArgs &a, float *p, cudaStream_t st);
+// cache_seqlens[i] += s_new for i < b.
+cudaError_t launch_kvcache_advance(int32_t *cache_seqlens, int b, int s_new, cudaStream_t st);
 
 }  // namespace attn

@@ -40,6 +40,8 @@ _SIGS = {
                          [_f, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
     "attn_fwd_kvcache_noalloc": ([_vp] * 7 + [_i] * 3 + [_vp, _vp] + [_i] * 7 +
                                  [_f, _i, _i, _i, _f, _i, _vp], _i),
+    "attn_fwd_probs": ([_vp] * 4 + [_i] * 7 + [_f, _i, _i, _i, _f, _vp], _i),
+    "attn_kvcache_advance": ([_vp, _i, _i, _vp], _i),
     "attn_get_device_error": ([_vp, ctypes.POINTER(_i)], _i),
     "attn_launch_count": ([], ctypes.c_ulonglong),
 }
@@ -269,3 +271,32 @@ def device_error() -> tuple[int, int]:
     detail = ctypes.c_int(0)
     st = lib().attn_get_device_error(_stream(), ctypes.byref(detail))
     return st, detail.value
+
+
+def fwd_probs(q, k, lse, *, scale=None, causal=False, window=(-1, -1), softcap=0.0, out=None):
+    """Debug only (Inference Cookbook FAQ Q9): the (b,hq,sq,sk) fp32 attention
+    probabilities of the forward that produced ``lse`` -- O(N^2) memory."""
+    torch = _torch()
+    b, sq, hq, d = q.shape
+    _, sk, hkv, _ = k.shape
+    _need(k.shape[0] == b and k.shape[3] == d, "k shape mismatch")
+    _need(q.dtype == k.dtype, "q, k must share a dtype")
+    _need(tuple(lse.shape) == (b, hq, sq) and lse.dtype == torch.float32, "lse must be (b,hq,sq) fp32")
+    out = torch.empty((b, hq, sq, sk), device=q.device, dtype=torch.float32) if out is None else out
+    _cuda_contig(q, k, lse, out)
+    wl, wr = _win(window)
+    st = lib().attn_fwd_probs(_p(q), _p(k), _p(lse), _p(out), _dt(q), b, sq, sk, hq, hkv, d,
+                              _scale(scale, d), int(bool(causal)), wl, wr, float(softcap),
+                              _stream())
+    _check(st, "attn_fwd_probs")
+    return out
+
+
+def kvcache_advance(cache_seqlens, s_new: int):
+    """cache_seqlens += s_new on the current stream (Inference Cookbook FAQ
+    Q17), as a kernel so a decode step can be captured in a CUDA graph (FAQ Q19)."""
+    torch = _torch()
+    _need(cache_seqlens.dtype == torch.int32, "cache_seqlens must be int32")
+    _cuda_contig(cache_seqlens)
+    st = lib().attn_kvcache_advance(_p(cache_seqlens), cache_seqlens.numel(), int(s_new), _stream())
+    _check(st, "attn_kvcache_advance")

@@ -204,6 +204,33 @@ attn_status attn_fwd_kvcache_noalloc(const void *q, void *k_cache, void *v_cache
                                      attn_stream_t stream);
 
 /*
+ * Debug only: the attention probabilities of a forward call (Inference
+ * Cookbook FAQ Q9, return_attn_probs: the whole (batch, heads, seqlen_q,
+ * seqlen_k) matrix costs O(N^2) memory, so it is for tests and debugging,
+ * never the hot path).  q (b,sq,hq,d), k (b,sk,hkv,d) in dtype and lse
+ * (b,hq,sq) fp32 as attn_fwd produced it for the same arguments.  p
+ * (b,hq,sq,sk) fp32 is fully overwritten: P_ij = exp(s_ij - LSE_i) for every
+ * visible (i, j), 0 elsewhere, with s the scaled (and soft-capped) score of
+ * attn_fwd, so each non-empty row sums to 1 and rows that see no key are 0.
+ * Same argument checks as attn_fwd; p must be 16-byte aligned.
+ */
+attn_status attn_fwd_probs(const void *q, const void *k, const float *lse, float *p, int dtype,
+                           int b, int sq, int sk, int hq, int hkv, int d, float scale,
+                           int causal, int win_l, int win_r, float softcap,
+                           attn_stream_t stream);
+
+/*
+ * cache_seqlens[i] += s_new for i in [0, b), as one kernel on `stream`.
+ * attn_fwd_kvcache appends k_new/v_new but never advances the lengths; the
+ * caller does (Inference Cookbook FAQ Q17).  Done on the device, the
+ * advance lets a whole decode step -- attn_fwd_kvcache then this call -- be
+ * captured once in a CUDA graph and replayed with fixed addresses (FAQ
+ * Q19).  cache_seqlens: device int32[b], 4-byte aligned.  b == 0 is a no-op;
+ * b < 0, s_new < 0 or a NULL array with b > 0 is ATTN_ERR_INVALID.
+ */
+attn_status attn_kvcache_advance(int32_t *cache_seqlens, int b, int s_new, attn_stream_t stream);
+
+/*
  * Reads and clears the sticky device error word of the current device
  * (synchronises `stream`; diagnostic use, not for the hot path).  Returns
  * ATTN_OK, ATTN_ERR_DEVICE or ATTN_ERR_TIMEOUT.  If `detail` is not NULL it

@@ -144,6 +144,25 @@ def forward_rows(q, k, v, samples, scale, causal=False, win_l=-1, win_r=-1, soft
     return o, lse
 
 
+def probs(q, k, scale, causal=False, win_l=-1, win_r=-1, softcap=0.0):
+    """The attention probability matrix P (b, hq, sq, sk) of a dense forward:
+    what Inference Cookbook FAQ Q9's return_attn_probs hands back (O(N^2)
+    memory, for debugging).  Row i is the softmax of the scaled, soft-capped
+    scores over the keys it may see, 0 elsewhere; rows that see no key are 0.
+    q (b,sq,hq,d), k (b,sk,hkv,d) float64.
+    """
+    b, sq, hq, d = q.shape
+    sk, hkv = k.shape[1], k.shape[2]
+    p = np.zeros((b, hq, sq, sk))
+    rows = np.arange(sq)
+    mask = visible(rows, sq, sk, causal, win_l, win_r)
+    for bi in range(b):
+        for h in range(hq):
+            s, _ = _scores(q[bi, :, h], k[bi, :, kv_head_of(h, hq, hkv)], scale, softcap)
+            p[bi, h], _ = _softmax_rows(s, mask)
+    return p
+
+
 def round_to(x, dtype):
     """Round float64 values to fp16 or bf16 (round to nearest even), as the
     forward's stored output is; returns float64."""

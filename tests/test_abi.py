@@ -92,3 +92,17 @@ def test_kvcache_argument_checks(lib):
     assert call(args(bt=None, num_pages=4)) == 1   # contiguous: one page per entry
     assert call(args(s_new=-1)) == 1
     assert call(args(b=0)) == 0
+
+
+def test_probs_and_advance_argument_checks(lib):
+    probs = lambda p=FAKE, b=1, hq=4, hkv=2, d=128: lib.attn_fwd_probs(
+        FAKE, FAKE, FAKE, p, 1, b, 8, 8, hq, hkv, d, 0.1, 0, -1, -1, 0.0, None)
+    assert probs(hq=6, hkv=4) == 1       # hq not a multiple of hkv
+    assert probs(d=96) == 2              # head dim not supported
+    assert probs(p=None) == 1            # no output
+    assert probs(b=0) == 0               # empty problem: no-op
+    assert lib.attn_kvcache_advance(FAKE, -1, 1, None) == 1
+    assert lib.attn_kvcache_advance(FAKE, 2, -1, None) == 1
+    assert lib.attn_kvcache_advance(None, 2, 1, None) == 1
+    assert lib.attn_kvcache_advance(ctypes.c_void_p(0x10002), 2, 1, None) == 1  # misaligned
+    assert lib.attn_kvcache_advance(FAKE, 0, 1, None) == 0

@@ -417,3 +417,27 @@ def test_stored_output_reading_of_d():
         assert np.abs(got[0] - exact[0]).max() > 0
     np.testing.assert_array_equal(ref.round_to(np.array([1.0, 1.00390625, 1.01171875]), "bf16"),
                                   [1.0, 1.0, 1.015625])
+
+
+@pytest.mark.parametrize("kw", [dict(causal=True), dict(win_l=2, win_r=1, softcap=3.0),
+                                dict(causal=True, win_l=1)])
+def test_probability_matrix_reproduces_forward(kw):
+    """FAQ Q9 debug matrix: O = P V row by row (against the separately pinned
+    forward), non-empty rows sum to 1, masked entries are exactly 0, and the
+    rows that see no key (sq > sk, bottom-right causal) are all zero."""
+    rng = np.random.default_rng(11)
+    b, sq, sk, hq, hkv, d = 2, 7, 5, 4, 2, 8
+    q, k, v = (rng.standard_normal(sh) for sh in ((b, sq, hq, d), (b, sk, hkv, d), (b, sk, hkv, d)))
+    p = ref.probs(q, k, 0.4, **kw)
+    o, lse = ref.forward(q, k, v, 0.4, **kw)
+    g = hq // hkv
+    for bi in range(b):
+        for h in range(hq):
+            np.testing.assert_allclose(p[bi, h] @ v[bi, :, h // g], o[bi, :, h], atol=1e-12)
+    mask = ref.visible(np.arange(sq), sq, sk, kw.get("causal", False), kw.get("win_l", -1),
+                       kw.get("win_r", -1))
+    assert np.all(p[:, :, ~mask] == 0.0)
+    nonempty = mask.any(axis=1)
+    np.testing.assert_allclose(p.sum(axis=3)[:, :, nonempty], 1.0, atol=1e-12)
+    assert np.all(p[:, :, ~nonempty] == 0.0)
+    assert np.all(np.isneginf(lse[:, :, ~nonempty]))
