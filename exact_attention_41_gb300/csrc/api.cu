@@ -58,6 +58,22 @@ attn_status check_common(int dtype, int hq, int hkv, int d, float scale, int win
   return ATTN_OK;
 }
 
+// Token strides in elements; 0 means contiguous (heads * d).  A given stride
+// must hold a whole row of heads and keep 16-byte alignment (TMA).
+bool stride_ok(int64_t rs, int heads, int d) {
+  return rs == 0 || (rs >= (int64_t)heads * d && rs % 8 == 0 && rs <= (int64_t)1 << 40);
+}
+void set_strides(FwdArgs &a, int64_t q_rs, int64_t k_rs, int64_t v_rs) {
+  a.q_rs = q_rs ? q_rs : (int64_t)a.hq * a.d;
+  a.k_rs = k_rs ? k_rs : (int64_t)a.hkv * a.d;
+  a.v_rs = v_rs ? v_rs : (int64_t)a.hkv * a.d;
+}
+void set_grad_strides(BwdArgs &a, int64_t dq_rs, int64_t dk_rs, int64_t dv_rs) {
+  a.dq_rs = dq_rs ? dq_rs : (int64_t)a.f.hq * a.f.d;
+  a.dk_rs = dk_rs ? dk_rs : (int64_t)a.f.hkv * a.f.d;
+  a.dv_rs = dv_rs ? dv_rs : (int64_t)a.f.hkv * a.f.d;
+}
+
 attn_status launched(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
 // Backward workspace for `rows` query rows in total: D_i (fp32, LSE
@@ -124,11 +140,16 @@ const char *attn_status_str(attn_status s) {
   return "unknown status";
 }
 
-attn_status attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
-                     int dtype, int b, int sq, int sk, int hq, int hkv, int d, float scale,
-                     int causal, int win_l, int win_r, float softcap, attn_stream_t stream) {
+attn_status attn_fwd_strided(const void *q, const void *k, const void *v, void *out, float *lse,
+                             int64_t q_row_stride, int64_t k_row_stride, int64_t v_row_stride,
+                             int dtype, int b, int sq, int sk, int hq, int hkv, int d,
+                             float scale, int causal, int win_l, int win_r, float softcap,
+                             attn_stream_t stream) {
   attn_status st = check_common(dtype, hq, hkv, d, scale, win_l, win_r, causal, softcap);
   if (st != ATTN_OK) return st;
+  if (!stride_ok(q_row_stride, hq, d) || !stride_ok(k_row_stride, hkv, d) ||
+      !stride_ok(v_row_stride, hkv, d))
+    return ATTN_ERR_INVALID;
   if (b < 0 || sq < 0 || sk < 0) return ATTN_ERR_INVALID;
   if (b == 0 || sq == 0) return ATTN_OK;
   if (!q || !out || !lse || (sk > 0 && (!k || !v))) return ATTN_ERR_INVALID;
@@ -140,7 +161,15 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *out, flo
   if (!di) return ATTN_ERR_CUDA;
   FwdArgs a{q, k, v, out, lse, Seqs{nullptr, nullptr, sq, sk, 0, 0, hq}, b, hq, hkv, d, dtype,
             scale, softcap > 0.f ? softcap : 0.f, win_l, win_r, di->err};
+  set_strides(a, q_row_stride, k_row_stride, v_row_stride);
   return launched(launch_fwd_tc(a, stream));
+}
+
+attn_status attn_fwd(const void *q, const void *k, const void *v, void *out, float *lse,
+                     int dtype, int b, int sq, int sk, int hq, int hkv, int d, float scale,
+                     int causal, int win_l, int win_r, float softcap, attn_stream_t stream) {
+  return attn_fwd_strided(q, k, v, out, lse, 0, 0, 0, dtype, b, sq, sk, hq, hkv, d, scale, causal,
+                          win_l, win_r, softcap, stream);
 }
 
 size_t attn_bwd_workspace_size(int b, int sq, int sk, int hq, int hkv, int d, int deterministic) {
@@ -149,13 +178,20 @@ size_t attn_bwd_workspace_size(int b, int sq, int sk, int hq, int hkv, int d, in
   return bwd_ws_bytes((int64_t)b * sq, hq, d, deterministic);
 }
 
-attn_status attn_bwd(const void *q, const void *k, const void *v, const void *out,
-                     const float *lse, const void *dout, void *dq, void *dk, void *dv,
-                     int dtype, int b, int sq, int sk, int hq, int hkv, int d, float scale,
-                     int causal, int win_l, int win_r, float softcap, int deterministic,
-                     void *workspace, size_t workspace_bytes, attn_stream_t stream) {
+attn_status attn_bwd_strided(const void *q, const void *k, const void *v, const void *out,
+                             const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                             int64_t q_row_stride, int64_t k_row_stride, int64_t v_row_stride,
+                             int64_t dq_row_stride, int64_t dk_row_stride,
+                             int64_t dv_row_stride, int dtype, int b, int sq, int sk, int hq,
+                             int hkv, int d, float scale, int causal, int win_l, int win_r,
+                             float softcap, int deterministic, void *workspace,
+                             size_t workspace_bytes, attn_stream_t stream) {
   attn_status st = check_common(dtype, hq, hkv, d, scale, win_l, win_r, causal, softcap);
   if (st != ATTN_OK) return st;
+  if (!stride_ok(q_row_stride, hq, d) || !stride_ok(k_row_stride, hkv, d) ||
+      !stride_ok(v_row_stride, hkv, d) || !stride_ok(dq_row_stride, hq, d) ||
+      !stride_ok(dk_row_stride, hkv, d) || !stride_ok(dv_row_stride, hkv, d))
+    return ATTN_ERR_INVALID;
   if (b < 0 || sq < 0 || sk < 0) return ATTN_ERR_INVALID;
   if (b == 0 || (sq == 0 && sk == 0)) return ATTN_OK;
   if ((sq > 0 && (!q || !out || !lse || !dout || !dq)) || (sk > 0 && (!k || !v || !dk || !dv)))
@@ -173,7 +209,19 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *ou
                     Seqs{nullptr, nullptr, sq, sk, 0, 0, hq}, b, hq, hkv, d, dtype, scale,
                     softcap > 0.f ? softcap : 0.f, win_l, win_r, di->err},
             dout, dq, dk, dv, nullptr, nullptr, nullptr, deterministic};
+  set_strides(a.f, q_row_stride, k_row_stride, v_row_stride);
+  set_grad_strides(a, dq_row_stride, dk_row_stride, dv_row_stride);
   return run_bwd(a, (int64_t)b * sq, workspace, di, stream);
+}
+
+attn_status attn_bwd(const void *q, const void *k, const void *v, const void *out,
+                     const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                     int dtype, int b, int sq, int sk, int hq, int hkv, int d, float scale,
+                     int causal, int win_l, int win_r, float softcap, int deterministic,
+                     void *workspace, size_t workspace_bytes, attn_stream_t stream) {
+  return attn_bwd_strided(q, k, v, out, lse, dout, dq, dk, dv, 0, 0, 0, 0, 0, 0, dtype, b, sq,
+                          sk, hq, hkv, d, scale, causal, win_l, win_r, softcap, deterministic,
+                          workspace, workspace_bytes, stream);
 }
 
 attn_status attn_fwd_varlen(const void *q, const void *k, const void *v, void *out, float *lse,
@@ -199,6 +247,7 @@ attn_status attn_fwd_varlen(const void *q, const void *k, const void *v, void *o
             Seqs{cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, total_q, total_k, hq},
             batch, hq, hkv, d, dtype, scale, softcap > 0.f ? softcap : 0.f, win_l, win_r,
             di->err};
+  set_strides(a, 0, 0, 0);
   return launched(launch_fwd_tc(a, stream));
 }
 
@@ -241,6 +290,8 @@ attn_status attn_bwd_varlen(const void *q, const void *k, const void *v, const v
                     batch, hq, hkv, d, dtype, scale, softcap > 0.f ? softcap : 0.f, win_l, win_r,
                     di->err},
             dout, dq, dk, dv, nullptr, nullptr, nullptr, deterministic};
+  set_strides(a.f, 0, 0, 0);
+  set_grad_strides(a, 0, 0, 0);
   return run_bwd(a, total_q, workspace, di, stream);
 }
 
@@ -322,6 +373,7 @@ attn_status attn_fwd_probs(const void *q, const void *k, const float *lse, float
   FwdArgs a{q, k, nullptr, nullptr, const_cast<float *>(lse),
             Seqs{nullptr, nullptr, sq, sk, 0, 0, hq}, b, hq, hkv, d, dtype, scale,
             softcap > 0.f ? softcap : 0.f, win_l, win_r, di->err};
+  set_strides(a, 0, 0, 0);
   return launched(launch_probs(a, p, stream));
 }
 

@@ -37,10 +37,10 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_rows_kernel(FwdArgs a) {
   int q0, lq, k0, lk;
   if (!a.seqs.get(b, q0, lq, k0, lk, a.err) || i >= lq) return;
   const int kvh = h / (a.hq / a.hkv);
-  const int64_t rs = (int64_t)a.hkv * D;
-  const T *qrow = static_cast<const T *>(a.q) + ((int64_t)(q0 + i) * a.hq + h) * D;
-  const T *kb = static_cast<const T *>(a.k) + (int64_t)k0 * rs + (int64_t)kvh * D;
-  const T *vb = static_cast<const T *>(a.v) + (int64_t)k0 * rs + (int64_t)kvh * D;
+  const int64_t krs = a.k_rs, vrs = a.v_rs;
+  const T *qrow = static_cast<const T *>(a.q) + (int64_t)(q0 + i) * a.q_rs + (int64_t)h * D;
+  const T *kb = static_cast<const T *>(a.k) + (int64_t)k0 * krs + (int64_t)kvh * D;
+  const T *vb = static_cast<const T *>(a.v) + (int64_t)k0 * vrs + (int64_t)kvh * D;
   for (int c = lane; c < D; c += 32) qs[warp][c] = Elem<T>::to_f(qrow[c]);
   __syncwarp();
   int lo, hi;
@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_rows_kernel(FwdArgs a) {
     const int j = j0 + lane;
     float s = -INFINITY;
     if (j <= hi) {
-      const float dot = dot_row<T, D>(qs[warp], kb + (int64_t)j * rs);
+      const float dot = dot_row<T, D>(qs[warp], kb + (int64_t)j * krs);
       s = a.softcap > 0.f ? a.softcap * tanhf(dot * a.scale / a.softcap) * kLog2e : dot * sl2;
     }
     const float mnew = fmaxf(m, warp_max(s));
@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_rows_kernel(FwdArgs a) {
     for (int jj = 0; jj < n; ++jj) {
       const float pj = __shfl_sync(0xffffffffu, p, jj);
       float vv[V];
-      load_vec<T, V>(vb + (int64_t)(j0 + jj) * rs + lane * V, vv);
+      load_vec<T, V>(vb + (int64_t)(j0 + jj) * vrs + lane * V, vv);
 #pragma unroll
       for (int u = 0; u < V; ++u) acc[u] = fmaf(pj, vv[u], acc[u]);
     }
@@ -113,13 +113,14 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_rows_kernel(BwdArgs a) {
   int q0, lq, k0, lk;
   if (!f.seqs.get(b, q0, lq, k0, lk, f.err) || i >= lq) return;
   const int kvh = h / (f.hq / f.hkv);
-  const int64_t rs = (int64_t)f.hkv * D;
-  const int64_t qoff = ((int64_t)(q0 + i) * f.hq + h) * D;
-  const T *kb = static_cast<const T *>(f.k) + (int64_t)k0 * rs + (int64_t)kvh * D;
-  const T *vb = static_cast<const T *>(f.v) + (int64_t)k0 * rs + (int64_t)kvh * D;
+  const int64_t krs = f.k_rs, vrs = f.v_rs;
+  const int64_t qoff = (int64_t)(q0 + i) * f.q_rs + (int64_t)h * D;      // q
+  const int64_t goff = ((int64_t)(q0 + i) * f.hq + h) * D;             // dO (contiguous)
+  const T *kb = static_cast<const T *>(f.k) + (int64_t)k0 * krs + (int64_t)kvh * D;
+  const T *vb = static_cast<const T *>(f.v) + (int64_t)k0 * vrs + (int64_t)kvh * D;
   for (int c = lane; c < D; c += 32) {
     qs[warp][c] = Elem<T>::to_f(static_cast<const T *>(f.q)[qoff + c]);
-    gs[warp][c] = Elem<T>::to_f(static_cast<const T *>(a.dout)[qoff + c]);
+    gs[warp][c] = Elem<T>::to_f(static_cast<const T *>(a.dout)[goff + c]);
   }
   __syncwarp();
   const int64_t li = f.seqs.lse_index(b, h, q0, i);
@@ -133,7 +134,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_rows_kernel(BwdArgs a) {
     const int j = j0 + lane;
     float ds = 0.f;
     if (j <= hi) {
-      const float s_raw = dot_row<T, D>(qs[warp], kb + (int64_t)j * rs) * f.scale;
+      const float s_raw = dot_row<T, D>(qs[warp], kb + (int64_t)j * krs) * f.scale;
       float s = s_raw, dcap = 1.f;
       if (f.softcap > 0.f) {
         const float t = tanhf(s_raw / f.softcap);
@@ -141,21 +142,22 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dq_rows_kernel(BwdArgs a) {
         dcap = 1.f - t * t;
       }
       const float p = exp2f(s * kLog2e - lse2);
-      const float dp = dot_row<T, D>(gs[warp], vb + (int64_t)j * rs);
+      const float dp = dot_row<T, D>(gs[warp], vb + (int64_t)j * vrs);
       ds = p * (dp - dsum) * dcap;
     }
     const int n = min(32, hi - j0 + 1);
     for (int jj = 0; jj < n; ++jj) {
       const float dj = __shfl_sync(0xffffffffu, ds, jj);
       float kk[V];
-      load_vec<T, V>(kb + (int64_t)(j0 + jj) * rs + lane * V, kk);
+      load_vec<T, V>(kb + (int64_t)(j0 + jj) * krs + lane * V, kk);
 #pragma unroll
       for (int u = 0; u < V; ++u) acc[u] = fmaf(dj, kk[u], acc[u]);
     }
   }
 #pragma unroll
   for (int u = 0; u < V; ++u) acc[u] *= f.scale;
-  store_vec<T, V>(static_cast<T *>(a.dq) + qoff + lane * V, acc);
+  store_vec<T, V>(static_cast<T *>(a.dq) + (int64_t)(q0 + i) * a.dq_rs + (int64_t)h * D + lane * V,
+                  acc);
 }
 
 // dV_j = sum_{h in group} sum_i P_ij dO_i and dK_j = scale * sum dS_ij q_i,
@@ -172,10 +174,10 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_rows_kernel(BwdArgs a) {
   int q0, lq, k0, lk;
   if (!f.seqs.get(b, q0, lq, k0, lk, f.err) || j >= lk) return;
   const int g = f.hq / f.hkv;
-  const int64_t koff = ((int64_t)(k0 + j) * f.hkv + kvh) * D;
+  const int64_t krow = (int64_t)(k0 + j), col = (int64_t)kvh * D;
   for (int c = lane; c < D; c += 32) {
-    ks[warp][c] = Elem<T>::to_f(static_cast<const T *>(f.k)[koff + c]);
-    vs[warp][c] = Elem<T>::to_f(static_cast<const T *>(f.v)[koff + c]);
+    ks[warp][c] = Elem<T>::to_f(static_cast<const T *>(f.k)[krow * f.k_rs + col + c]);
+    vs[warp][c] = Elem<T>::to_f(static_cast<const T *>(f.v)[krow * f.v_rs + col + c]);
   }
   __syncwarp();
   int lo, hi;
@@ -185,15 +187,15 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_rows_kernel(BwdArgs a) {
   for (int u = 0; u < V; ++u) dk[u] = dv[u] = 0.f;
   for (int t = 0; t < g; ++t) {
     const int h = kvh * g + t;
-    const T *qb = static_cast<const T *>(f.q) + ((int64_t)q0 * f.hq + h) * D;
+    const T *qb = static_cast<const T *>(f.q) + (int64_t)q0 * f.q_rs + (int64_t)h * D;
     const T *gb = static_cast<const T *>(a.dout) + ((int64_t)q0 * f.hq + h) * D;
-    const int64_t rs = (int64_t)f.hq * D;
+    const int64_t qrs = f.q_rs, grs = (int64_t)f.hq * D;
     for (int i0 = lo; i0 <= hi; i0 += 32) {
       const int i = i0 + lane;
       float p = 0.f, ds = 0.f;
       if (i <= hi) {
         const int64_t li = f.seqs.lse_index(b, h, q0, i);
-        const float s_raw = dot_row<T, D>(ks[warp], qb + (int64_t)i * rs) * f.scale;
+        const float s_raw = dot_row<T, D>(ks[warp], qb + (int64_t)i * qrs) * f.scale;
         float s = s_raw, dcap = 1.f;
         if (f.softcap > 0.f) {
           const float tt = tanhf(s_raw / f.softcap);
@@ -201,7 +203,7 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_rows_kernel(BwdArgs a) {
           dcap = 1.f - tt * tt;
         }
         p = exp2f(s * kLog2e - f.lse[li] * kLog2e);
-        const float dp = dot_row<T, D>(vs[warp], gb + (int64_t)i * rs);
+        const float dp = dot_row<T, D>(vs[warp], gb + (int64_t)i * grs);
         ds = p * (dp - a.dsum[li]) * dcap;
       }
       const int n = min(32, hi - i0 + 1);
@@ -209,8 +211,8 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_rows_kernel(BwdArgs a) {
         const float pi = __shfl_sync(0xffffffffu, p, ii);
         const float di = __shfl_sync(0xffffffffu, ds, ii);
         float gg[V], qq[V];
-        load_vec<T, V>(gb + (int64_t)(i0 + ii) * rs + lane * V, gg);
-        load_vec<T, V>(qb + (int64_t)(i0 + ii) * rs + lane * V, qq);
+        load_vec<T, V>(gb + (int64_t)(i0 + ii) * grs + lane * V, gg);
+        load_vec<T, V>(qb + (int64_t)(i0 + ii) * qrs + lane * V, qq);
 #pragma unroll
         for (int u = 0; u < V; ++u) {
           dv[u] = fmaf(pi, gg[u], dv[u]);
@@ -221,8 +223,8 @@ __global__ void __launch_bounds__(kWarps * 32) bwd_dkdv_rows_kernel(BwdArgs a) {
   }
 #pragma unroll
   for (int u = 0; u < V; ++u) dk[u] *= f.scale;
-  store_vec<T, V>(static_cast<T *>(a.dk) + koff + lane * V, dk);
-  store_vec<T, V>(static_cast<T *>(a.dv) + koff + lane * V, dv);
+  store_vec<T, V>(static_cast<T *>(a.dk) + krow * a.dk_rs + col + lane * V, dk);
+  store_vec<T, V>(static_cast<T *>(a.dv) + krow * a.dv_rs + col + lane * V, dv);
 }
 
 template <typename T, int D>

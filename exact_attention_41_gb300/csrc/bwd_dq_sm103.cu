@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     if (ok) {
-      T *row = static_cast<T *>(a.dq) + ((int64_t)(q0 + (valid ? i : 0)) * f.hq + h) * D;
+      T *row = static_cast<T *>(a.dq) + (int64_t)(q0 + (valid ? i : 0)) * a.dq_rs + (int64_t)h * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t u[32];
@@ -314,12 +314,13 @@ cudaError_t bwd_dq(const BwdArgs &a, cudaStream_t st) {
   const int64_t rows_q = f.seqs.cu_q ? f.seqs.total_q : (int64_t)f.batch * f.seqs.sq;
   const int64_t rows_k = f.seqs.cu_k ? f.seqs.total_k : (int64_t)f.batch * f.seqs.sk;
   if (rows_q == 0) return cudaSuccess;
-  if (rows_k == 0) return cudaMemsetAsync(a.dq, 0, (size_t)rows_q * f.hq * D * 2, st);
+  if (rows_k == 0)
+    return cudaMemset2DAsync(a.dq, (size_t)a.dq_rs * 2, 0, (size_t)f.hq * D * 2, (size_t)rows_q, st);
   CUtensorMap tq, tk, tv, tdo;
-  if (!make_map_3d(&tq, f.q, f.dtype, rows_q, f.hq, D, BM) ||
+  if (!make_map_3d(&tq, f.q, f.dtype, rows_q, f.hq, D, BM, f.q_rs) ||
       !make_map_3d(&tdo, a.dout, f.dtype, rows_q, f.hq, D, BM) ||
-      !make_map_3d(&tk, f.k, f.dtype, rows_k, f.hkv, D, BN) ||
-      !make_map_3d(&tv, f.v, f.dtype, rows_k, f.hkv, D, BN))
+      !make_map_3d(&tk, f.k, f.dtype, rows_k, f.hkv, D, BN, f.k_rs) ||
+      !make_map_3d(&tv, f.v, f.dtype, rows_k, f.hkv, D, BN, f.v_rs))
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem_once<bwd_dq_kernel<T>>(kSmem);
   if (e != cudaSuccess) return e;

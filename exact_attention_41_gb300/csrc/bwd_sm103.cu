@@ -464,9 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     // tcgen05.ld is warp-collective: every lane loads, only real keys store
     if (ok) {
-      const int64_t off = ((int64_t)(k0 + kj) * f.hkv + kvh) * D;
-      T *dvr = static_cast<T *>(a.dv) + off;
-      T *dkr = static_cast<T *>(a.dk) + off;
+      T *dvr = static_cast<T *>(a.dv) + (int64_t)(k0 + kj) * a.dv_rs + (int64_t)kvh * D;
+      T *dkr = static_cast<T *>(a.dk) + (int64_t)(k0 + kj) * a.dk_rs + (int64_t)kvh * D;
 #pragma unroll 1
       for (int c = 2 * w; c < 2 * w + 2; ++c) {
 #pragma unroll
@@ -562,7 +561,14 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdArgs a, int64_t 
     const float4 v = reinterpret_cast<const float4 *>(a.dq_acc)[x];
     const float s = a.f.scale;
     uint2 out{Elem<T>::from_f2(v.x * s, v.y * s), Elem<T>::from_f2(v.z * s, v.w * s)};
-    reinterpret_cast<uint2 *>(a.dq)[x] = out;
+    // the accumulator is contiguous (rows, hq * d); dQ rows are dq_rs apart
+    const int64_t per_row = (int64_t)a.f.hq * D / 4;
+    int64_t dst = x * 4;
+    if (a.dq_rs != per_row * 4) {
+      const int64_t row = x / per_row;
+      dst = row * a.dq_rs + (x - row * per_row) * 4;
+    }
+    *reinterpret_cast<uint2 *>(static_cast<T *>(a.dq) + dst) = out;
   }
 }
 
@@ -578,10 +584,10 @@ cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
   }
   if (rows_k > 0 && rows_q > 0) {
     CUtensorMap tq, tk, tv, tdo;
-    if (!make_map_3d(&tq, f.q, f.dtype, rows_q, f.hq, D, BQ) ||
+    if (!make_map_3d(&tq, f.q, f.dtype, rows_q, f.hq, D, BQ, f.q_rs) ||
         !make_map_3d(&tdo, a.dout, f.dtype, rows_q, f.hq, D, BQ) ||
-        !make_map_3d(&tk, f.k, f.dtype, rows_k, f.hkv, D, BN) ||
-        !make_map_3d(&tv, f.v, f.dtype, rows_k, f.hkv, D, BN))
+        !make_map_3d(&tk, f.k, f.dtype, rows_k, f.hkv, D, BN, f.k_rs) ||
+        !make_map_3d(&tv, f.v, f.dtype, rows_k, f.hkv, D, BN, f.v_rs))
       return cudaErrorInvalidValue;
     cudaError_t e = set_smem_once<bwd_tc_kernel<T>>(kSmem);
     if (e != cudaSuccess) return e;
@@ -591,9 +597,9 @@ cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
     bwd_tc_kernel<T><<<(unsigned)grid, kThreads, kSmem, st>>>(tq, tk, tv, tdo, a, n_blocks);
     count_launches(1);
   } else if (rows_k > 0) {  // no queries: the key gradients are zero
-    const size_t bytes = (size_t)rows_k * f.hkv * D * 2;
-    cudaError_t e = cudaMemsetAsync(a.dk, 0, bytes, st);
-    if (e == cudaSuccess) e = cudaMemsetAsync(a.dv, 0, bytes, st);
+    const size_t w = (size_t)f.hkv * D * 2;
+    cudaError_t e = cudaMemset2DAsync(a.dk, (size_t)a.dk_rs * 2, 0, w, (size_t)rows_k, st);
+    if (e == cudaSuccess) e = cudaMemset2DAsync(a.dv, (size_t)a.dv_rs * 2, 0, w, (size_t)rows_k, st);
     if (e != cudaSuccess) return e;
   }
   if (a.deterministic) {

@@ -43,11 +43,12 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // (rows, heads, D) tensor, box {64, 1, box_rows}, 128-byte swizzle.
 bool make_map_3d(CUtensorMap *m, const void *base, int dtype, int64_t rows, int heads, int d,
-              int box_rows) {
+              int box_rows, int64_t row_stride) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)heads * d * 2};
+  if (row_stride == 0) row_stride = (int64_t)heads * d;
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)row_stride * 2};
   cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
@@ -464,9 +465,9 @@ cudaError_t fwd_tc(const FwdArgs &a, cudaStream_t st) {
   const int64_t rows_k = a.seqs.cu_k ? a.seqs.total_k : (int64_t)a.batch * a.seqs.sk;
   if (rows_k == 0) return launch_fwd_simt(a, st);  // no keys: every row is empty
   CUtensorMap tq, tk, tv;
-  if (!make_map_3d(&tq, a.q, a.dtype, rows_q, a.hq, D, kBM) ||
-      !make_map_3d(&tk, a.k, a.dtype, rows_k, a.hkv, D, BN) ||
-      !make_map_3d(&tv, a.v, a.dtype, rows_k, a.hkv, D, BN))
+  if (!make_map_3d(&tq, a.q, a.dtype, rows_q, a.hq, D, kBM, a.q_rs) ||
+      !make_map_3d(&tk, a.k, a.dtype, rows_k, a.hkv, D, BN, a.k_rs) ||
+      !make_map_3d(&tv, a.v, a.dtype, rows_k, a.hkv, D, BN, a.v_rs))
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem_once<fwd_tc_kernel<T, D, BN, NT>>(C::kSmem);
   if (e != cudaSuccess) return e;

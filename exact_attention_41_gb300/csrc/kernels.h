@@ -19,6 +19,10 @@ struct FwdArgs {
   float scale, softcap;  // softcap <= 0: off
   int win_l, win_r;      // -1 = unbounded; causal already folded into win_r = 0
   int *err;              // device error word
+  // elements between consecutive tokens of q, k, v (row r of head h starts
+  // at r * stride + h * d); hq*d / hkv*d when contiguous, larger for packed
+  // qkv / kv layouts.  Set by the C ABI before any launch.
+  int64_t q_rs, k_rs, v_rs;
 };
 
 struct BwdArgs {
@@ -29,6 +33,7 @@ struct BwdArgs {
   float2 *lsd;           // workspace: (LSE_i * log2(e), D_i), LSE layout (tensor-core path)
   float *dq_acc;         // workspace: fp32 dQ accumulator (atomic mode)
   int deterministic;
+  int64_t dq_rs, dk_rs, dv_rs;  // token strides of the gradients (as q_rs ...)
 };
 
 struct DecodeArgs {
@@ -51,8 +56,9 @@ struct DecodeArgs {
 // cuTensorMapEncodeTiled from the driver (looked up once), or nullptr.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // 3-D (rows, heads, d) tensor map, box {64, 1, box_rows}, 128-byte swizzle.
+// row_stride: elements between consecutive rows (0: heads * d, contiguous).
 bool make_map_3d(CUtensorMap *m, const void *base, int dtype, int64_t rows, int heads, int d,
-                 int box_rows);
+                 int box_rows, int64_t row_stride = 0);
 // dQ of the backward, query-stationary (d = 128): written once, no atomics.
 cudaError_t launch_bwd_dq_tc(const BwdArgs &a, cudaStream_t st);
 // Tensor-core decode; cudaErrorNotSupported for shapes it does not handle.

@@ -29,7 +29,11 @@ _SIGS = {
     "attn_version": ([], ctypes.c_char_p),
     "attn_status_str": ([_i], ctypes.c_char_p),
     "attn_fwd": ([_vp] * 5 + [_i] * 7 + [_f, _i, _i, _i, _f, _vp], _i),
+    "attn_fwd_strided": ([_vp] * 5 + [ctypes.c_int64] * 3 + [_i] * 7 + [_f, _i, _i, _i, _f, _vp],
+                         _i),
     "attn_bwd_workspace_size": ([_i] * 7, _sz),
+    "attn_bwd_strided": ([_vp] * 9 + [ctypes.c_int64] * 6 + [_i] * 7 +
+                         [_f, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
     "attn_bwd": ([_vp] * 9 + [_i] * 7 + [_f, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
     "attn_fwd_varlen": ([_vp] * 7 + [_i] * 9 + [_f, _i, _i, _i, _f, _vp], _i),
     "attn_bwd_varlen_workspace_size": ([_i] * 9, _sz),
@@ -127,21 +131,54 @@ def _scale(scale, d):
     return 1.0 / math.sqrt(d) if scale is None else float(scale)
 
 
+def _row_stride(t):
+    """Token stride (elements) of a (b, s, h, d) tensor whose heads are dense
+    within a token: 0 when fully contiguous, the stride when it is a view of a
+    packed layout (e.g. qkv[:, :, 0] of a (b, s, 3, h, d) tensor)."""
+    if t is None or t.is_contiguous():
+        return 0
+    b, s, h, d = t.shape
+    _need(t.is_cuda, "tensors must be on a CUDA device")
+    _need(t.stride(3) == 1 and t.stride(2) == d and (b == 1 or t.stride(0) == s * t.stride(1)),
+          "a non-contiguous q/k/v must be a token-strided view with dense heads "
+          "(e.g. of a packed (b, s, 3, h, d) tensor)")
+    return t.stride(1)
+
+
 def fwd(q, k, v, *, scale=None, causal=False, window=(-1, -1), softcap=0.0, out=None, lse=None):
-    """Dense forward.  q (b,sq,hq,d), k/v (b,sk,hkv,d) -> out (b,sq,hq,d), lse (b,hq,sq) fp32."""
+    """Dense forward.  q (b,sq,hq,d), k/v (b,sk,hkv,d) -> out (b,sq,hq,d), lse (b,hq,sq) fp32.
+    q/k/v may be token-strided views of packed qkv / kv tensors (no copies)."""
     torch = _torch()
     b, sq, hq, d = q.shape
     _, sk, hkv, _ = k.shape
     _need(k.shape == v.shape and k.shape[0] == b and k.shape[3] == d, "k/v shape mismatch")
     _need(q.dtype == k.dtype == v.dtype, "q, k, v must share a dtype")
-    out = torch.empty_like(q) if out is None else out
+    out = torch.empty_like(q, memory_format=torch.contiguous_format) if out is None else out
     lse = torch.empty((b, hq, sq), device=q.device, dtype=torch.float32) if lse is None else lse
-    _cuda_contig(q, k, v, out, lse)
+    rs = [_row_stride(t) for t in (q, k, v)]
+    _cuda_contig(out, lse)
     wl, wr = _win(window)
-    st = lib().attn_fwd(_p(q), _p(k), _p(v), _p(out), _p(lse), _dt(q), b, sq, sk, hq, hkv, d,
-                        _scale(scale, d), int(bool(causal)), wl, wr, float(softcap), _stream())
+    args = (_dt(q), b, sq, sk, hq, hkv, d, _scale(scale, d), int(bool(causal)), wl, wr,
+            float(softcap), _stream())
+    if any(rs):
+        st = lib().attn_fwd_strided(_p(q), _p(k), _p(v), _p(out), _p(lse), *rs, *args)
+    else:
+        _cuda_contig(q, k, v)
+        st = lib().attn_fwd(_p(q), _p(k), _p(v), _p(out), _p(lse), *args)
     _check(st, "attn_fwd")
     return out, lse
+
+
+def fwd_qkvpacked(qkv, **kw):
+    """Forward on a packed (b, s, 3, h, d) tensor ("flash_attn FlashAttention
+    完整说明" §六.1's qkvpacked call), read in place."""
+    return fwd(qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2], **kw)
+
+
+def fwd_kvpacked(q, kv, **kw):
+    """Forward with a packed (b, sk, 2, hkv, d) key/value tensor (Inference
+    Cookbook FAQ Q7's kvpacked call), read in place."""
+    return fwd(q, kv[:, :, 0], kv[:, :, 1], **kw)
 
 
 def bwd_workspace(q, k, deterministic=False):
@@ -157,18 +194,34 @@ def bwd(q, k, v, out, lse, dout, *, scale=None, causal=False, window=(-1, -1), s
     torch = _torch()
     b, sq, hq, d = q.shape
     _, sk, hkv, _ = k.shape
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
+    cf = torch.contiguous_format
+    dq = torch.empty_like(q, memory_format=cf) if dq is None else dq
+    dk = torch.empty_like(k, memory_format=cf) if dk is None else dk
+    dv = torch.empty_like(v, memory_format=cf) if dv is None else dv
     ws = bwd_workspace(q, k, deterministic) if workspace is None else workspace
-    _cuda_contig(q, k, v, out, lse, dout, dq, dk, dv, ws)
+    rs = [_row_stride(t) for t in (q, k, v, dq, dk, dv)]
+    _cuda_contig(out, lse, dout, ws)
     wl, wr = _win(window)
-    st = lib().attn_bwd(_p(q), _p(k), _p(v), _p(out), _p(lse), _p(dout), _p(dq), _p(dk), _p(dv),
-                        _dt(q), b, sq, sk, hq, hkv, d, _scale(scale, d), int(bool(causal)), wl,
-                        wr, float(softcap), int(bool(deterministic)), _p(ws), ws.numel(),
-                        _stream())
+    ptrs = (_p(q), _p(k), _p(v), _p(out), _p(lse), _p(dout), _p(dq), _p(dk), _p(dv))
+    args = (_dt(q), b, sq, sk, hq, hkv, d, _scale(scale, d), int(bool(causal)), wl, wr,
+            float(softcap), int(bool(deterministic)), _p(ws), ws.numel(), _stream())
+    if any(rs):
+        st = lib().attn_bwd_strided(*ptrs, *rs, *args)
+    else:
+        _cuda_contig(q, k, v, dq, dk, dv)
+        st = lib().attn_bwd(*ptrs, *args)
     _check(st, "attn_bwd")
     return dq, dk, dv
+
+
+def bwd_qkvpacked(qkv, out, lse, dout, *, dqkv=None, **kw):
+    """Backward of fwd_qkvpacked: the gradients land in a packed (b, s, 3, h, d)
+    tensor ``dqkv`` (allocated if not given) with no copies."""
+    torch = _torch()
+    dqkv = torch.empty_like(qkv) if dqkv is None else dqkv
+    bwd(qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2], out, lse, dout,
+        dq=dqkv[:, :, 0], dk=dqkv[:, :, 1], dv=dqkv[:, :, 2], **kw)
+    return dqkv
 
 
 def fwd_varlen(q, k, v, cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, *, scale=None,

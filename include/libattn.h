@@ -108,6 +108,37 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *ou
                      void *workspace, size_t workspace_bytes, attn_stream_t stream);
 
 /*
+ * attn_fwd / attn_bwd for inputs (and, in the backward, gradients) whose
+ * tokens are not densely packed: *_row_stride is the number of elements from
+ * token r to token r + 1 of that tensor (row r = batch * s + position; head
+ * h of a row starts h * d elements after the row; batch entries follow each
+ * other at s rows).  0 means contiguous (heads * d).  This takes the packed
+ * layouts without copies -- qkv (b, s, 3, hq, d) of the qkvpacked call
+ * ("flash_attn FlashAttention完整说明" §六.1): q = qkv, k = qkv + hq*d,
+ * v = qkv + 2*hq*d, every stride 3*hq*d; kv (b, s, 2, hkv, d) of the
+ * kvpacked call (Inference Cookbook FAQ Q7): k = kv, v = kv + hkv*d, both
+ * strides 2*hkv*d -- and writes the gradients into the same packed layout.
+ * out, lse and dout stay contiguous.  A non-zero stride must be at least
+ * heads * d and a multiple of 8 (16-byte rows); every pointer 16-byte
+ * aligned; otherwise ATTN_ERR_INVALID.  Everything else as attn_fwd /
+ * attn_bwd.
+ */
+attn_status attn_fwd_strided(const void *q, const void *k, const void *v, void *out, float *lse,
+                             int64_t q_row_stride, int64_t k_row_stride, int64_t v_row_stride,
+                             int dtype, int b, int sq, int sk, int hq, int hkv, int d,
+                             float scale, int causal, int win_l, int win_r, float softcap,
+                             attn_stream_t stream);
+
+attn_status attn_bwd_strided(const void *q, const void *k, const void *v, const void *out,
+                             const float *lse, const void *dout, void *dq, void *dk, void *dv,
+                             int64_t q_row_stride, int64_t k_row_stride, int64_t v_row_stride,
+                             int64_t dq_row_stride, int64_t dk_row_stride,
+                             int64_t dv_row_stride, int dtype, int b, int sq, int sk, int hq,
+                             int hkv, int d, float scale, int causal, int win_l, int win_r,
+                             float softcap, int deterministic, void *workspace,
+                             size_t workspace_bytes, attn_stream_t stream);
+
+/*
  * Varlen (packed) forward, Inference Cookbook FAQ Q8.  q (total_q,hq,d),
  * k/v (total_k,hkv,d), out (total_q,hq,d); lse (hq,total_q) fp32.
  * cu_seqlens_q/k: DEVICE int32 arrays of batch+1 offsets starting at 0.

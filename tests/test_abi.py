@@ -106,3 +106,17 @@ def test_probs_and_advance_argument_checks(lib):
     assert lib.attn_kvcache_advance(None, 2, 1, None) == 1
     assert lib.attn_kvcache_advance(ctypes.c_void_p(0x10002), 2, 1, None) == 1  # misaligned
     assert lib.attn_kvcache_advance(FAKE, 0, 1, None) == 0
+
+
+def test_strided_argument_checks(lib):
+    def fwd_s(qs=0, ks=0, vs=0):
+        return lib.attn_fwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, qs, ks, vs, 1, 1, 8, 8, 4, 2,
+                                    128, 0.1, 0, -1, -1, 0.0, None)
+    assert fwd_s(qs=4 * 128 - 8) == 1     # a token row shorter than its heads
+    assert fwd_s(ks=2 * 128 + 4) == 1     # not a multiple of 8 elements
+    assert fwd_s(vs=-8) == 1
+    bwd_s = lambda dk: lib.attn_bwd_strided(*([FAKE] * 9), 0, 0, 0, 0, dk, 0, 1, 1, 8, 8, 4, 2,
+                                            128, 0.1, 0, -1, -1, 0.0, 0, FAKE, 1 << 30, None)
+    assert bwd_s(2 * 128 - 8) == 1
+    assert lib.attn_fwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, 3 * 4 * 128, 0, 0, 1, 0, 8, 8, 4, 2,
+                                128, 0.1, 0, -1, -1, 0.0, None) == 0   # empty: no-op
