@@ -2,12 +2,12 @@
 
     python -m exact_attention_41_gb300.profile_case fwd     # b=1 s=8192 hq=16 hkv=4 d=128 causal
     python -m exact_attention_41_gb300.profile_case bwd
-    python -m exact_attention_41_gb300.profile_case decode  # b=16 sq=4, 4096-token caches
+    python -m exact_attention_41_gb300.profile_case decode  # b=8 sq=4, caches U[1,32768]
 
 Each runs `--calls` calls (default 2: one warm-up, one to capture) and checks
 the device error word.  Inputs are seeded N(0,1) bf16 drawn on the device;
-the problems are larger than L2 in their K/V or Q/dO streams but a few
-hundred MB in total.
+the problems are larger than L2 in their K/V or Q/dO streams and at most
+about 1 GB in total.
 """
 from __future__ import annotations
 
@@ -48,8 +48,8 @@ def main():
             for _ in range(args.calls):
                 libattn.bwd(q, k, v, o, lse, do, causal=True, deterministic=args.deterministic)
     else:
-        b, sq, page = 16, 4, 256
-        seqlens, table, npages = syn.decode_layout(9, b, 4096, page, sq)
+        b, sq, page = 8, 4, 256
+        seqlens, table, npages = syn.decode_layout(9, b, 32768, page, sq)
         kc = syn.device_normal((npages, page, args.hkv * 2, d), bf, 5)
         vc = syn.device_normal((npages, page, args.hkv * 2, d), bf, 6)
         q = syn.device_normal((b, sq, args.hkv * 8, d), bf, 7)
