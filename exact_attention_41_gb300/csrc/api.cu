@@ -74,6 +74,20 @@ void set_grad_strides(BwdArgs &a, int64_t dq_rs, int64_t dk_rs, int64_t dv_rs) {
   a.dv_rs = dv_rs ? dv_rs : (int64_t)a.f.hkv * a.f.d;
 }
 
+// PackGQA (Inference Cookbook FAQ Q15): the g = hq / hkv query heads of a
+// KV head share every 128-row tile of the forward.  pack_gqa < 0: automatic
+// -- on when the query sequences are short (<= 128 rows, where an unpacked
+// 256-row query block is mostly empty), off for long ones, where the FAQ
+// notes packing can be slightly slower; 0: off; > 0: on.  Returns the pack
+// factor, or 0 when packing is asked for but g does not divide 128.
+int resolve_pack(int pack_gqa, int hq, int hkv, int max_sq) {
+  const int g = hq / hkv;
+  const bool can = g > 1 && 128 % g == 0;
+  if (pack_gqa == 0 || g == 1) return 1;
+  if (pack_gqa > 0) return can ? g : 0;
+  return can && max_sq <= 128 ? g : 1;
+}
+
 attn_status launched(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
 // Backward workspace for `rows` query rows in total: D_i (fp32, LSE
@@ -144,7 +158,7 @@ attn_status attn_fwd_strided(const void *q, const void *k, const void *v, void *
                              int64_t q_row_stride, int64_t k_row_stride, int64_t v_row_stride,
                              int dtype, int b, int sq, int sk, int hq, int hkv, int d,
                              float scale, int causal, int win_l, int win_r, float softcap,
-                             attn_stream_t stream) {
+                             int pack_gqa, attn_stream_t stream) {
   attn_status st = check_common(dtype, hq, hkv, d, scale, win_l, win_r, causal, softcap);
   if (st != ATTN_OK) return st;
   if (!stride_ok(q_row_stride, hq, d) || !stride_ok(k_row_stride, hkv, d) ||
@@ -157,11 +171,14 @@ attn_status attn_fwd_strided(const void *q, const void *k, const void *v, void *
     return ATTN_ERR_INVALID;
   if ((int64_t)b * sq * hq > INT32_MAX || (int64_t)b * sk * hkv > INT32_MAX)
     return ATTN_ERR_UNSUPPORTED;
+  const int pack = resolve_pack(pack_gqa, hq, hkv, sq);
+  if (pack == 0) return ATTN_ERR_UNSUPPORTED;
   const DeviceInfo *di = device_info();
   if (!di) return ATTN_ERR_CUDA;
   FwdArgs a{q, k, v, out, lse, Seqs{nullptr, nullptr, sq, sk, 0, 0, hq}, b, hq, hkv, d, dtype,
             scale, softcap > 0.f ? softcap : 0.f, win_l, win_r, di->err};
   set_strides(a, q_row_stride, k_row_stride, v_row_stride);
+  a.pack = pack;
   return launched(launch_fwd_tc(a, stream));
 }
 
@@ -169,7 +186,7 @@ attn_status attn_fwd(const void *q, const void *k, const void *v, void *out, flo
                      int dtype, int b, int sq, int sk, int hq, int hkv, int d, float scale,
                      int causal, int win_l, int win_r, float softcap, attn_stream_t stream) {
   return attn_fwd_strided(q, k, v, out, lse, 0, 0, 0, dtype, b, sq, sk, hq, hkv, d, scale, causal,
-                          win_l, win_r, softcap, stream);
+                          win_l, win_r, softcap, -1, stream);
 }
 
 size_t attn_bwd_workspace_size(int b, int sq, int sk, int hq, int hkv, int d, int deterministic) {
@@ -248,6 +265,7 @@ attn_status attn_fwd_varlen(const void *q, const void *k, const void *v, void *o
             batch, hq, hkv, d, dtype, scale, softcap > 0.f ? softcap : 0.f, win_l, win_r,
             di->err};
   set_strides(a, 0, 0, 0);
+  a.pack = resolve_pack(-1, hq, hkv, max_seqlen_q);
   return launched(launch_fwd_tc(a, stream));
 }
 

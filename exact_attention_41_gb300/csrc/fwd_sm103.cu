@@ -43,13 +43,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // (rows, heads, D) tensor, box {64, 1, box_rows}, 128-byte swizzle.
 bool make_map_3d(CUtensorMap *m, const void *base, int dtype, int64_t rows, int heads, int d,
-              int box_rows, int64_t row_stride) {
+              int box_rows, int64_t row_stride, int box_heads) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
   if (row_stride == 0) row_stride = (int64_t)heads * d;
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)row_stride * 2};
-  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
              3, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -131,17 +131,24 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
   uint8_t *v_s = k_s + ST * C::kKVBytes;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // CTA -> (query block, batch, head): heaviest blocks first, heads fastest.
+  // PackGQA (Inference Cookbook FAQ Q15): with pg = g, tile row r holds
+  // position r / pg of the tile and query head r % pg of the KV head's group.
+  const int pg = a.pack > 1 ? a.pack : 1;
+  const int tile_pos = kBM / pg;  // query positions per 128-row tile
+  // CTA -> (query block, batch, head or KV head): heaviest blocks first,
+  // heads fastest.
+  const int nh = pg > 1 ? a.hkv : a.hq;
   const int bid = blockIdx.x;
-  const int h = bid % a.hq;
-  const int b = (bid / a.hq) % a.batch;
-  const int mb = m_blocks - 1 - bid / (a.hq * a.batch);
+  const int hh = bid % nh;
+  const int b = (bid / nh) % a.batch;
+  const int mb = m_blocks - 1 - bid / (nh * a.batch);
   int q0, lq, k0, lk;
   if (!a.seqs.get(b, q0, lq, k0, lk, a.err)) return;
-  const int m0 = mb * (kBM * NT);
+  const int m0 = mb * (tile_pos * NT);  // first query position of the CTA
   if (m0 >= lq) return;
-  const int kvh = h / (a.hq / a.hkv);
-  const int m_last = min(m0 + kBM * NT, lq) - 1;
+  const int kvh = pg > 1 ? hh : hh / (a.hq / a.hkv);
+  const int h = pg > 1 ? kvh * pg : hh;  // (first) query head of the tile rows
+  const int m_last = min(m0 + tile_pos * NT, lq) - 1;
 
   // key tiles any row of this query block may see
   int lo_first, hi_first, lo_last, hi_last;
@@ -195,7 +202,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
       for (int t = 0; t < NT; ++t)
         for (int c = 0; c < D / 64; ++c)
           tma_load_3d(q_s + t * C::kQBytes + c * kBM * 128, &tq, &sh.q_full, c * 64, h,
-                      q0 + m0 + t * kBM);
+                      q0 + m0 + t * tile_pos);
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
         const int st = j % ST;
@@ -317,16 +324,17 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
     if constexpr (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
     // ------------------------------------------------------------ softmax
     const int t = (warp - C::kSoftmaxWarp0) >> 2;  // query tile of this warpgroup
-    const int r = 32 * (warp & 3) + lane;  // TMEM lane = query row in the tile
-    const int i = m0 + t * kBM + r;
+    const int r = 32 * (warp & 3) + lane;  // TMEM lane = row in the tile
+    const int i = m0 + t * tile_pos + r / pg;  // its query position
+    const int hr = h + r % pg;                 // and query head
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     const uint32_t o_t = tmem + lane_off + t * D;
     int lo_i, hi_i;
     key_range(i, lq, lk, a.win_l, a.win_r, lo_i, hi_i);
     // tiles that need no mask: every row of the tile sees every key in them
     int lo_tile_max, hi_tile_min, dummy;
-    key_range(m0 + t * kBM + kBM - 1, lq, lk, a.win_l, a.win_r, lo_tile_max, dummy);
-    key_range(m0 + t * kBM, lq, lk, a.win_l, a.win_r, dummy, hi_tile_min);
+    key_range(m0 + t * tile_pos + tile_pos - 1, lq, lk, a.win_l, a.win_r, lo_tile_max, dummy);
+    key_range(m0 + t * tile_pos, lq, lk, a.win_l, a.win_r, dummy, hi_tile_min);
     const float sl2 = a.scale * kLog2e;
     const bool cap = a.softcap > 0.f;
     const float cap_in = cap ? a.scale / a.softcap : 0.f, cap_out = a.softcap * kLog2e;
@@ -425,7 +433,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
     tc_fence_after();
     if (ok) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      T *orow = static_cast<T *>(a.o) + ((int64_t)(q0 + i) * a.hq + h) * D;
+      T *orow = static_cast<T *>(a.o) + ((int64_t)(q0 + i) * a.hq + hr) * D;
       const bool valid = i < lq;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
@@ -449,7 +457,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
       }
       if (valid) {
         const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-        a.lse[a.seqs.lse_index(b, h, q0, i)] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
+        a.lse[a.seqs.lse_index(b, hr, q0, i)] = l > 0.f ? (m_use + __log2f(l)) * kLn2 : -INFINITY;
       }
     }
   }
@@ -465,14 +473,17 @@ cudaError_t fwd_tc(const FwdArgs &a, cudaStream_t st) {
   const int64_t rows_k = a.seqs.cu_k ? a.seqs.total_k : (int64_t)a.batch * a.seqs.sk;
   if (rows_k == 0) return launch_fwd_simt(a, st);  // no keys: every row is empty
   CUtensorMap tq, tk, tv;
-  if (!make_map_3d(&tq, a.q, a.dtype, rows_q, a.hq, D, kBM, a.q_rs) ||
+  const int pg = a.pack > 1 ? a.pack : 1;
+  if (kBM % pg != 0) return cudaErrorInvalidValue;
+  if (!make_map_3d(&tq, a.q, a.dtype, rows_q, a.hq, D, kBM / pg, a.q_rs, pg) ||
       !make_map_3d(&tk, a.k, a.dtype, rows_k, a.hkv, D, BN, a.k_rs) ||
       !make_map_3d(&tv, a.v, a.dtype, rows_k, a.hkv, D, BN, a.v_rs))
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem_once<fwd_tc_kernel<T, D, BN, NT>>(C::kSmem);
   if (e != cudaSuccess) return e;
-  const int m_blocks = (a.seqs.sq + kBM * NT - 1) / (kBM * NT);
-  const int64_t grid = (int64_t)m_blocks * a.hq * a.batch;
+  const int block_pos = kBM / pg * NT;  // query positions per CTA
+  const int m_blocks = (a.seqs.sq + block_pos - 1) / block_pos;
+  const int64_t grid = (int64_t)m_blocks * (pg > 1 ? a.hkv : a.hq) * a.batch;
   if (grid == 0) return cudaSuccess;
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
   fwd_tc_kernel<T, D, BN, NT><<<(unsigned)grid, C::kThreads, C::kSmem, st>>>(tq, tk, tv, a,

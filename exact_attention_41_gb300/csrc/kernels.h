@@ -23,6 +23,9 @@ struct FwdArgs {
   // at r * stride + h * d); hq*d / hkv*d when contiguous, larger for packed
   // qkv / kv layouts.  Set by the C ABI before any launch.
   int64_t q_rs, k_rs, v_rs;
+  // PackGQA: 1, or g = hq / hkv when the g query heads of one KV head share
+  // every 128-row tile (128 / g positions x g heads).  Set by the C ABI.
+  int pack;
 };
 
 struct BwdArgs {
@@ -55,10 +58,11 @@ struct DecodeArgs {
 
 // cuTensorMapEncodeTiled from the driver (looked up once), or nullptr.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
-// 3-D (rows, heads, d) tensor map, box {64, 1, box_rows}, 128-byte swizzle.
+// 3-D (rows, heads, d) tensor map, box {64, box_heads, box_rows}, 128-byte
+// swizzle (a box lands as box_rows * box_heads rows of 128 bytes, head-minor).
 // row_stride: elements between consecutive rows (0: heads * d, contiguous).
 bool make_map_3d(CUtensorMap *m, const void *base, int dtype, int64_t rows, int heads, int d,
-                 int box_rows, int64_t row_stride = 0);
+                 int box_rows, int64_t row_stride = 0, int box_heads = 1);
 // dQ of the backward, query-stationary (d = 128): written once, no atomics.
 cudaError_t launch_bwd_dq_tc(const BwdArgs &a, cudaStream_t st);
 // Tensor-core decode; cudaErrorNotSupported for shapes it does not handle.

@@ -29,8 +29,8 @@ _SIGS = {
     "attn_version": ([], ctypes.c_char_p),
     "attn_status_str": ([_i], ctypes.c_char_p),
     "attn_fwd": ([_vp] * 5 + [_i] * 7 + [_f, _i, _i, _i, _f, _vp], _i),
-    "attn_fwd_strided": ([_vp] * 5 + [ctypes.c_int64] * 3 + [_i] * 7 + [_f, _i, _i, _i, _f, _vp],
-                         _i),
+    "attn_fwd_strided": ([_vp] * 5 + [ctypes.c_int64] * 3 + [_i] * 7 +
+                         [_f, _i, _i, _i, _f, _i, _vp], _i),
     "attn_bwd_workspace_size": ([_i] * 7, _sz),
     "attn_bwd_strided": ([_vp] * 9 + [ctypes.c_int64] * 6 + [_i] * 7 +
                          [_f, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
@@ -145,9 +145,11 @@ def _row_stride(t):
     return t.stride(1)
 
 
-def fwd(q, k, v, *, scale=None, causal=False, window=(-1, -1), softcap=0.0, out=None, lse=None):
+def fwd(q, k, v, *, scale=None, causal=False, window=(-1, -1), softcap=0.0, out=None, lse=None,
+        pack_gqa=None):
     """Dense forward.  q (b,sq,hq,d), k/v (b,sk,hkv,d) -> out (b,sq,hq,d), lse (b,hq,sq) fp32.
-    q/k/v may be token-strided views of packed qkv / kv tensors (no copies)."""
+    q/k/v may be token-strided views of packed qkv / kv tensors (no copies).
+    pack_gqa: None = automatic, False/True = off/on (Inference Cookbook FAQ Q15)."""
     torch = _torch()
     b, sq, hq, d = q.shape
     _, sk, hkv, _ = k.shape
@@ -160,8 +162,10 @@ def fwd(q, k, v, *, scale=None, causal=False, window=(-1, -1), softcap=0.0, out=
     wl, wr = _win(window)
     args = (_dt(q), b, sq, sk, hq, hkv, d, _scale(scale, d), int(bool(causal)), wl, wr,
             float(softcap), _stream())
-    if any(rs):
-        st = lib().attn_fwd_strided(_p(q), _p(k), _p(v), _p(out), _p(lse), *rs, *args)
+    if any(rs) or pack_gqa is not None:
+        pk = -1 if pack_gqa is None else int(bool(pack_gqa))
+        st = lib().attn_fwd_strided(_p(q), _p(k), _p(v), _p(out), _p(lse), *rs, *args[:-1], pk,
+                                    args[-1])
     else:
         _cuda_contig(q, k, v)
         st = lib().attn_fwd(_p(q), _p(k), _p(v), _p(out), _p(lse), *args)

@@ -122,12 +122,20 @@ attn_status attn_bwd(const void *q, const void *k, const void *v, const void *ou
  * heads * d and a multiple of 8 (16-byte rows); every pointer 16-byte
  * aligned; otherwise ATTN_ERR_INVALID.  Everything else as attn_fwd /
  * attn_bwd.
+ *
+ * pack_gqa (forward; Inference Cookbook FAQ Q15): with GQA, the g = hq/hkv
+ * query heads of a KV head may share each 128-row tile (128/g positions x g
+ * heads), so short query sequences do not leave tiles empty and each K/V
+ * tile serves g heads.  < 0: automatic (on when sq <= 128 and g divides 128,
+ * which is what attn_fwd and attn_fwd_varlen use); 0: off; > 0: on, and
+ * ATTN_ERR_UNSUPPORTED when g does not divide 128.  The result does not
+ * depend on the choice.
  */
 attn_status attn_fwd_strided(const void *q, const void *k, const void *v, void *out, float *lse,
                              int64_t q_row_stride, int64_t k_row_stride, int64_t v_row_stride,
                              int dtype, int b, int sq, int sk, int hq, int hkv, int d,
                              float scale, int causal, int win_l, int win_r, float softcap,
-                             attn_stream_t stream);
+                             int pack_gqa, attn_stream_t stream);
 
 attn_status attn_bwd_strided(const void *q, const void *k, const void *v, const void *out,
                              const float *lse, const void *dout, void *dq, void *dk, void *dv,

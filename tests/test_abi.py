@@ -111,7 +111,7 @@ def test_probs_and_advance_argument_checks(lib):
 def test_strided_argument_checks(lib):
     def fwd_s(qs=0, ks=0, vs=0):
         return lib.attn_fwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, qs, ks, vs, 1, 1, 8, 8, 4, 2,
-                                    128, 0.1, 0, -1, -1, 0.0, None)
+                                    128, 0.1, 0, -1, -1, 0.0, -1, None)
     assert fwd_s(qs=4 * 128 - 8) == 1     # a token row shorter than its heads
     assert fwd_s(ks=2 * 128 + 4) == 1     # not a multiple of 8 elements
     assert fwd_s(vs=-8) == 1
@@ -119,4 +119,7 @@ def test_strided_argument_checks(lib):
                                             128, 0.1, 0, -1, -1, 0.0, 0, FAKE, 1 << 30, None)
     assert bwd_s(2 * 128 - 8) == 1
     assert lib.attn_fwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, 3 * 4 * 128, 0, 0, 1, 0, 8, 8, 4, 2,
-                                128, 0.1, 0, -1, -1, 0.0, None) == 0   # empty: no-op
+                                128, 0.1, 0, -1, -1, 0.0, -1, None) == 0   # empty: no-op
+    # PackGQA forced on needs hq / hkv to divide the 128-row tile
+    assert lib.attn_fwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 0, 1, 1, 8, 8, 6, 2,
+                                128, 0.1, 0, -1, -1, 0.0, 1, None) == 2

@@ -74,3 +74,55 @@ def test_kvpacked_gqa_cross_attention(d):
     assert_close(host(out), ro, dtype, "out")
     assert_lse(host(lse), rl)
     _check_grads(dq, dkv[:, :, 0], dkv[:, :, 1], c, dtype, d, kw)
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+@pytest.mark.parametrize("sq,sk,hq,hkv,kw", [
+    (16, 300, 8, 2, dict(causal=True)),                      # short queries: auto packs
+    (5, 5, 16, 2, dict(causal=True)),                        # g = 8: 16 positions per tile
+    (130, 257, 16, 1, dict(window=(40, 3), softcap=6.0)),    # g = 16, ragged, forced on
+    (300, 200, 8, 2, dict(causal=True)),                     # sq > sk: leading rows empty
+])
+def test_pack_gqa_matches_oracle_and_unpacked(d, sq, sk, hq, hkv, kw):
+    """PackGQA (Inference Cookbook FAQ Q15): g query heads share each tile.
+    Forced on, off and automatic give the oracle's result, and the packed and
+    unpacked kernels agree bitwise (each row's arithmetic is the same)."""
+    import torch
+
+    from exact_attention_41_gb300 import libattn
+
+    dtype, b = syn.BF16, 2
+    c = syn.dense_case(63, b, sq, sk, hq, hkv, d, dtype)
+    q, k, v = (dev(c[n], dtype) for n in ("q", "k", "v"))
+    o1, l1 = libattn.fwd(q, k, v, pack_gqa=True, **kw)
+    o0, l0 = libattn.fwd(q, k, v, pack_gqa=False, **kw)
+    oa, la = libattn.fwd(q, k, v, **kw)
+    torch.cuda.synchronize()
+    win = kw.get("window", (-1, -1))
+    ro, rl = ref.forward(f64(c["q"], dtype), f64(c["k"], dtype), f64(c["v"], dtype),
+                         1 / math.sqrt(d), kw.get("causal", False), win[0], win[1],
+                         kw.get("softcap", 0.0))
+    for o, l, what in ((o1, l1, "packed"), (o0, l0, "unpacked"), (oa, la, "auto")):
+        assert_close(host(o), ro, dtype, f"out ({what})")
+        assert_lse(host(l), rl, f"lse ({what})")
+    assert torch.equal(o1, o0) and torch.equal(l1, l0)
+
+
+def test_pack_gqa_varlen_short_sequences():
+    """Varlen with every sequence <= 128 queries packs automatically."""
+    import torch
+
+    from exact_attention_41_gb300 import libattn
+
+    dtype, hq, hkv, d = syn.F16, 8, 2, 128
+    lens = np.array([1, 37, 128, 64, 100])
+    cu = syn.cu_seqlens(lens)
+    c = syn.varlen_case(64, lens, lens, hq, hkv, d, dtype)
+    q, k, v = (dev(c[n], dtype) for n in ("q", "k", "v"))
+    cu_d = torch.from_numpy(cu).cuda()
+    o, lse = libattn.fwd_varlen(q, k, v, cu_d, cu_d, int(lens.max()), int(lens.max()), causal=True)
+    torch.cuda.synchronize()
+    ro, rl = ref.varlen_forward(f64(c["q"], dtype), f64(c["k"], dtype), f64(c["v"], dtype), cu, cu,
+                                1 / math.sqrt(d), True)
+    assert_close(host(o), ro, dtype, "varlen out")
+    assert_lse(host(lse), rl)
