@@ -395,6 +395,46 @@ attn_status attn_fwd_probs(const void *q, const void *k, const float *lse, float
   return launched(launch_probs(a, p, stream));
 }
 
+size_t attn_fwd_fp8_workspace_size(int b, int sk, int hkv, int d) {
+  if (b <= 0 || sk <= 0 || hkv <= 0 || d <= 0) return 0;
+  return align256(sizeof(uint16_t) * (size_t)b * sk * hkv * d);  // v widened to bf16
+}
+
+attn_status attn_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *lse,
+                         float descale_q, float descale_k, float descale_v, int b, int sq, int sk,
+                         int hq, int hkv, int d, float scale, int causal, int win_l, int win_r,
+                         float softcap, void *workspace, size_t workspace_bytes,
+                         attn_stream_t stream) {
+  attn_status st = check_common(ATTN_BF16, hq, hkv, d, scale, win_l, win_r, causal, softcap);
+  if (st != ATTN_OK) return st;
+  for (float s : {descale_q, descale_k, descale_v})
+    if (!isfinite(s) || !(s > 0.f)) return ATTN_ERR_INVALID;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (b < 0 || sq < 0 || sk < 0) return ATTN_ERR_INVALID;
+  if (b == 0 || sq == 0) return ATTN_OK;
+  if (sk == 0) return ATTN_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !out || !lse) return ATTN_ERR_INVALID;
+  for (const void *p : {q, k, v, (const void *)out, (const void *)lse, (const void *)workspace})
+    if (!aligned16(p)) return ATTN_ERR_INVALID;
+  if ((int64_t)b * sq * hq > INT32_MAX || (int64_t)b * sk * hkv > INT32_MAX)
+    return ATTN_ERR_UNSUPPORTED;
+  const float eff = scale * descale_q * descale_k;
+  if (!isfinite(eff)) return ATTN_ERR_INVALID;
+  const size_t need = attn_fwd_fp8_workspace_size(b, sk, hkv, d);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+  const DeviceInfo *di = device_info();
+  if (!di) return ATTN_ERR_CUDA;
+  cudaError_t e = launch_widen_e4m3(v, workspace, (int64_t)b * sk * hkv * d, di->sms, stream);
+  if (e != cudaSuccess) return ATTN_ERR_CUDA;
+  FwdArgs a{q, k, workspace, out, lse, Seqs{nullptr, nullptr, sq, sk, 0, 0, hq}, b, hq, hkv, d,
+            ATTN_BF16, eff, softcap > 0.f ? softcap : 0.f, win_l, win_r, di->err};
+  set_strides(a, 0, 0, 0);
+  a.pack = resolve_pack(-1, hq, hkv, sq);
+  a.qk_fp8 = 1;
+  a.out_scale = descale_v;
+  return launched(launch_fwd_tc(a, stream));
+}
+
 attn_status attn_kvcache_advance(int32_t *cache_seqlens, int b, int s_new, attn_stream_t stream) {
   if (b < 0 || s_new < 0) return ATTN_ERR_INVALID;
   if (b == 0) return ATTN_OK;

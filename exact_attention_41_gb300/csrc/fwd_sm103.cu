@@ -48,10 +48,14 @@ bool make_map_3d(CUtensorMap *m, const void *base, int dtype, int64_t rows, int 
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)heads, (cuuint64_t)rows};
   if (row_stride == 0) row_stride = (int64_t)heads * d;
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)row_stride * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_heads, (cuuint32_t)box_rows};
+  // E4M3 tensors: 1-byte elements, so a 128-byte box row is 128 of them
+  const int eb = dtype == kDtypeE4M3 ? 1 : 2;
+  cuuint64_t strides[2] = {(cuuint64_t)d * eb, (cuuint64_t)row_stride * eb};
+  cuuint32_t box[3] = {(cuuint32_t)(128 / eb), (cuuint32_t)box_heads, (cuuint32_t)box_rows};
   cuuint32_t es[3] = {1, 1, 1};
-  return enc(m, dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+  return enc(m, dtype == kDtypeE4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+             : dtype == ATTN_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                  : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
              3, const_cast<void *>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -68,11 +72,14 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when max gro
 // between the tiles so one tile's softmax overlaps the other tile's MMAs, and
 // every K/V tile staged in shared memory serves 256 query rows.  NT = 1
 // (d = 256): TMEM = [O | S_a | S_b], S double-buffered instead.
-template <int D, int BN, int NT>
+// QB: bytes per Q/K element (2, or 1 for the E4M3 forward, whose V is bf16).
+template <int D, int BN, int NT, int QB = 2>
 struct FwdCfg {
   static constexpr int kStages = (D == 64) ? 3 : 2;
-  static constexpr int kQBytes = kBM * D * 2;  // one tile
-  static constexpr int kKVBytes = BN * D * 2;
+  static constexpr int kQBytes = kBM * D * QB;  // one tile
+  static constexpr int kKBytes = BN * D * QB;   // one K tile
+  static constexpr int kKVBytes = BN * D * 2;   // one stage slot (V is 16-bit)
+  static constexpr int kQKCols = D * QB / 128;  // 128-byte column blocks of Q / K
   static constexpr int kSmemData = NT * kQBytes + 2 * kStages * kKVBytes;
   // at least ~120 KB so that one CTA owns the SM (and all 512 TMEM columns)
   static constexpr int kSmem = (kSmemData + 1024 > 120 * 1024 ? kSmemData + 1024 : 120 * 1024);
@@ -116,11 +123,11 @@ template <> struct IsBf16<__nv_bfloat16> { static constexpr int v = 1; };
 template <typename T>
 __device__ __forceinline__ uint32_t pack2(float a, float b) { return Elem<T>::from_f2(a, b); }
 
-template <typename T, int D, int BN, int NT>
-__global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
+template <typename T, int D, int BN, int NT, int QB>
+__global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdArgs a, const int m_blocks) {
-  using C = FwdCfg<D, BN, NT>;
+  using C = FwdCfg<D, BN, NT, QB>;
   constexpr int ST = C::kStages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
@@ -200,8 +207,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
       prefetch_tmap(&tv);
       mbar_expect_tx(&sh.q_full, NT * C::kQBytes);
       for (int t = 0; t < NT; ++t)
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(q_s + t * C::kQBytes + c * kBM * 128, &tq, &sh.q_full, c * 64, h,
+        for (int c = 0; c < C::kQKCols; ++c)  // 128-byte column blocks
+          tma_load_3d(q_s + t * C::kQBytes + c * kBM * 128, &tq, &sh.q_full, c * (128 / QB), h,
                       q0 + m0 + t * tile_pos);
       int issued = 0;
       for (int j = 0; j < nt; ++j) {
@@ -209,10 +216,10 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
         const uint32_t ph = (j / ST) & 1;
         const int krow = k0 + (n_lo + j) * BN;
         if (!wait_bar(sh, &sh.k_empty[st], ph ^ 1, a.err)) break;
-        mbar_expect_tx(&sh.k_full[st], C::kKVBytes);
-        for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(k_s + st * C::kKVBytes + c * BN * 128, &tk, &sh.k_full[st], c * 64, kvh,
-                      krow);
+        mbar_expect_tx(&sh.k_full[st], C::kKBytes);
+        for (int c = 0; c < C::kQKCols; ++c)
+          tma_load_3d(k_s + st * C::kKVBytes + c * BN * 128, &tk, &sh.k_full[st], c * (128 / QB),
+                      kvh, krow);
         if (!wait_bar(sh, &sh.v_empty[st], ph ^ 1, a.err)) { issued = 2 * j + 1; break; }
         mbar_expect_tx(&sh.v_full[st], C::kKVBytes);
         for (int c = 0; c < D / 64; ++c)
@@ -234,20 +241,25 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
     // ------------------------------------------------------------ MMA issuer
     if (elect_one()) {
       constexpr int ab = IsBf16<T>::v;
-      constexpr uint32_t id_s = idesc_f16(kBM, BN, ab, 0, 0);
+      constexpr uint32_t id_s = QB == 1 ? idesc_e4m3(kBM, BN) : idesc_f16(kBM, BN, ab, 0, 0);
       constexpr uint32_t id_o = idesc_f16(kBM, D, ab, 0, 1);
       const uint32_t q_addr = smem_u32(q_s), k_addr = smem_u32(k_s), v_addr = smem_u32(v_s);
       // descriptor bases; every operand below is base + constant offset
       const uint64_t q_d = smem_desc(q_addr, 16, 1024), k_d = smem_desc(k_addr, 16, 1024);
       const uint64_t v_d = smem_desc(v_addr, BN * 128, 1024);
       // S_t = Q_t K_j^T into TMEM column `dcol`
+      // (each instruction takes 32 bytes of every row: 16 elements at 16 bits,
+      // 32 at 8 bits)
       auto mma_s = [&](int t, int j, uint32_t dcol) {
         const uint32_t ko = (j % ST) * C::kKVBytes;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < D * QB / 32; ++kk) {
           const uint64_t ad = desc_add(q_d, t * C::kQBytes + (kk / 4) * (kBM * 128) + (kk % 4) * 32);
           const uint64_t bd = desc_add(k_d, ko + (kk / 4) * (BN * 128) + (kk % 4) * 32);
-          mma_ss(dcol, ad, bd, id_s, kk > 0);
+          if constexpr (QB == 1)
+            mma_ss_e4m3(dcol, ad, bd, id_s, kk > 0);
+          else
+            mma_ss(dcol, ad, bd, id_s, kk > 0);
         }
       };
       // O_t += P V_j with P read from TMEM column `pcol`
@@ -432,7 +444,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     if (ok) {
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      // (out_scale: the V descale of the FP8 forward)
+      const float inv = l > 0.f ? (a.out_scale > 0.f ? a.out_scale : 1.f) / l : 0.f;
       T *orow = static_cast<T *>(a.o) + ((int64_t)(q0 + i) * a.hq + hr) * D;
       const bool valid = i < lq;
 #pragma unroll 1
@@ -466,27 +479,28 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT>::kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <typename T, int D, int BN, int NT>
+template <typename T, int D, int BN, int NT, int QB = 2>
 cudaError_t fwd_tc(const FwdArgs &a, cudaStream_t st) {
-  using C = FwdCfg<D, BN, NT>;
+  using C = FwdCfg<D, BN, NT, QB>;
+  const int qk_dtype = QB == 1 ? kDtypeE4M3 : a.dtype;
   const int64_t rows_q = a.seqs.cu_q ? a.seqs.total_q : (int64_t)a.batch * a.seqs.sq;
   const int64_t rows_k = a.seqs.cu_k ? a.seqs.total_k : (int64_t)a.batch * a.seqs.sk;
   if (rows_k == 0) return launch_fwd_simt(a, st);  // no keys: every row is empty
   CUtensorMap tq, tk, tv;
   const int pg = a.pack > 1 ? a.pack : 1;
   if (kBM % pg != 0) return cudaErrorInvalidValue;
-  if (!make_map_3d(&tq, a.q, a.dtype, rows_q, a.hq, D, kBM / pg, a.q_rs, pg) ||
-      !make_map_3d(&tk, a.k, a.dtype, rows_k, a.hkv, D, BN, a.k_rs) ||
+  if (!make_map_3d(&tq, a.q, qk_dtype, rows_q, a.hq, D, kBM / pg, a.q_rs, pg) ||
+      !make_map_3d(&tk, a.k, qk_dtype, rows_k, a.hkv, D, BN, a.k_rs) ||
       !make_map_3d(&tv, a.v, a.dtype, rows_k, a.hkv, D, BN, a.v_rs))
     return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_once<fwd_tc_kernel<T, D, BN, NT>>(C::kSmem);
+  cudaError_t e = set_smem_once<fwd_tc_kernel<T, D, BN, NT, QB>>(C::kSmem);
   if (e != cudaSuccess) return e;
   const int block_pos = kBM / pg * NT;  // query positions per CTA
   const int m_blocks = (a.seqs.sq + block_pos - 1) / block_pos;
   const int64_t grid = (int64_t)m_blocks * (pg > 1 ? a.hkv : a.hq) * a.batch;
   if (grid == 0) return cudaSuccess;
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
-  fwd_tc_kernel<T, D, BN, NT><<<(unsigned)grid, C::kThreads, C::kSmem, st>>>(tq, tk, tv, a,
+  fwd_tc_kernel<T, D, BN, NT, QB><<<(unsigned)grid, C::kThreads, C::kSmem, st>>>(tq, tk, tv, a,
                                                                           m_blocks);
   count_launches(1);
   return cudaGetLastError();
@@ -498,7 +512,9 @@ cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t st) {
   const bool bf = a.dtype == ATTN_BF16;
   switch (a.d) {
     case 64: return bf ? fwd_tc<__nv_bfloat16, 64, 128, 2>(a, st) : fwd_tc<__half, 64, 128, 2>(a, st);
-    case 128: return bf ? fwd_tc<__nv_bfloat16, 128, 128, 2>(a, st) : fwd_tc<__half, 128, 128, 2>(a, st);
+    case 128:
+      if (a.qk_fp8) return bf ? fwd_tc<__nv_bfloat16, 128, 128, 2, 1>(a, st) : cudaErrorInvalidValue;
+      return bf ? fwd_tc<__nv_bfloat16, 128, 128, 2>(a, st) : fwd_tc<__half, 128, 128, 2>(a, st);
     case 256: return bf ? fwd_tc<__nv_bfloat16, 256, 64, 1>(a, st) : fwd_tc<__half, 256, 64, 1>(a, st);
   }
   return cudaErrorInvalidValue;

@@ -26,7 +26,15 @@ struct FwdArgs {
   // PackGQA: 1, or g = hq / hkv when the g query heads of one KV head share
   // every 128-row tile (128 / g positions x g heads).  Set by the C ABI.
   int pack;
+  // FP8 forward: q and k hold E4M3 values (S runs as kind::f8f6f4), v is the
+  // bf16 widening of E4M3 values, and the output is multiplied by out_scale
+  // (the V descale).  0 / 0.f: the plain 16-bit forward.
+  int qk_fp8;
+  float out_scale;
 };
+
+// Storage code of E4M3 tensors for make_map_3d (beside ATTN_F16 / ATTN_BF16).
+constexpr int kDtypeE4M3 = 2;
 
 struct BwdArgs {
   FwdArgs f;             // f.o / f.lse are the forward's outputs (read only)
@@ -94,6 +102,8 @@ cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t st);
 cudaError_t launch_bwd_tc(const BwdArgs &a, int sms, cudaStream_t st);
 cudaError_t launch_bwd_simt(const BwdArgs &a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
+// E4M3 -> bf16 widening of n (a multiple of 16) contiguous values.
+cudaError_t launch_widen_e4m3(const void *src, void *dst, int64_t n, int sms, cudaStream_t st);
 // Debug probability matrix p (b, hq, sq, sk) fp32 from q, k and a.lse.
 cudaError_t launch_probs(const FwdArgs &a, float *p, cudaStream_t st);
 // cache_seqlens[i] += s_new for i < b.

@@ -44,6 +44,8 @@ _SIGS = {
                          [_f, _i, _i, _i, _f, _i, _vp, _sz, _vp], _i),
     "attn_fwd_kvcache_noalloc": ([_vp] * 7 + [_i] * 3 + [_vp, _vp] + [_i] * 7 +
                                  [_f, _i, _i, _i, _f, _i, _vp], _i),
+    "attn_fwd_fp8_workspace_size": ([_i] * 4, _sz),
+    "attn_fwd_fp8": ([_vp] * 5 + [_f] * 3 + [_i] * 6 + [_f, _i, _i, _i, _f, _vp, _sz, _vp], _i),
     "attn_fwd_probs": ([_vp] * 4 + [_i] * 7 + [_f, _i, _i, _i, _f, _vp], _i),
     "attn_kvcache_advance": ([_vp, _i, _i, _vp], _i),
     "attn_get_device_error": ([_vp, ctypes.POINTER(_i)], _i),
@@ -357,3 +359,28 @@ def kvcache_advance(cache_seqlens, s_new: int):
     _cuda_contig(cache_seqlens)
     st = lib().attn_kvcache_advance(_p(cache_seqlens), cache_seqlens.numel(), int(s_new), _stream())
     _check(st, "attn_kvcache_advance")
+
+
+def fwd_fp8(q, k, v, descale_q=1.0, descale_k=1.0, descale_v=1.0, *, scale=None, causal=False,
+            window=(-1, -1), softcap=0.0, out=None, lse=None, workspace=None):
+    """FP8 forward (Inference Cookbook FAQ Q20): q, k, v are float8_e4m3fn (or
+    uint8 E4M3 bytes) standing for q*descale_q etc.; returns bf16 out and fp32 lse."""
+    torch = _torch()
+    b, sq, hq, d = q.shape
+    _, sk, hkv, _ = k.shape
+    _need(k.shape == v.shape and k.shape[0] == b and k.shape[3] == d, "k/v shape mismatch")
+    for t in (q, k, v):
+        _need(t.element_size() == 1, "q, k, v must be 1-byte E4M3 tensors")
+    out = torch.empty((b, sq, hq, d), device=q.device, dtype=torch.bfloat16) if out is None else out
+    lse = torch.empty((b, hq, sq), device=q.device, dtype=torch.float32) if lse is None else lse
+    if workspace is None:
+        n = lib().attn_fwd_fp8_workspace_size(b, sk, hkv, d)
+        workspace = torch.empty(max(n, 1), device=q.device, dtype=torch.uint8)
+    _cuda_contig(q, k, v, out, lse, workspace)
+    wl, wr = _win(window)
+    st = lib().attn_fwd_fp8(_p(q), _p(k), _p(v), _p(out), _p(lse), float(descale_q),
+                            float(descale_k), float(descale_v), b, sq, sk, hq, hkv, d,
+                            _scale(scale, d), int(bool(causal)), wl, wr, float(softcap),
+                            _p(workspace), workspace.numel(), _stream())
+    _check(st, "attn_fwd_fp8")
+    return out, lse

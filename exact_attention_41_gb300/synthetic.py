@@ -45,6 +45,46 @@ def bits_to_f64(bits: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
+E4M3 = "e4m3"  # OCP FP8 E4M3 ("fn": no infinities, 0x7F/0xFF are NaN, max 448)
+
+
+def e4m3_values() -> np.ndarray:
+    """The float64 value of every E4M3 bit pattern 0..255 (NaN for 0x7F, 0xFF):
+    sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent field 0 is
+    subnormal (m/8 * 2^-6)."""
+    b = np.arange(256)
+    e = (b >> 3) & 0xF
+    m = (b & 7).astype(np.float64)
+    mag = np.where(e == 0, m / 8.0 * 2.0 ** -6, (1.0 + m / 8.0) * 2.0 ** (e - 7.0))
+    val = np.where(b & 0x80, -mag, mag)
+    val[(b & 0x7F) == 0x7F] = np.nan
+    return val
+
+
+def e4m3_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """Exact widening of E4M3 bit patterns (uint8) to float64."""
+    return e4m3_values()[np.asarray(bits, dtype=np.uint8)]
+
+
+def round_e4m3(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest E4M3 value (ties to the even pattern), saturating
+    magnitudes above 448 to 448; returns uint8 bit patterns."""
+    x = np.asarray(x, dtype=np.float64)
+    pos = e4m3_values()[:0x7F]                      # 0x00..0x7E, increasing
+    a = np.minimum(np.abs(x), pos[-1])
+    i = np.clip(np.searchsorted(pos, a), 1, len(pos) - 1)
+    lo, hi = pos[i - 1], pos[i]
+    take_hi = (a - lo > hi - a) | ((a - lo == hi - a) & ((i & 1) == 0))
+    code = np.where(take_hi, i, i - 1).astype(np.uint8)
+    code = np.where(a == 0, 0, code).astype(np.uint8)
+    return np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
+
+
+def normal_e4m3(rng: np.random.Generator, shape) -> np.ndarray:
+    """N(0,1) draws rounded to E4M3; returns uint8 bits."""
+    return round_e4m3(rng.standard_normal(size=shape, dtype=np.float32))
+
+
 def normal_bits(rng: np.random.Generator, shape, dtype: str) -> np.ndarray:
     """N(0,1) float32 draws rounded to ``dtype``; returns uint16 bits."""
     return round_bits(rng.standard_normal(size=shape, dtype=np.float32), dtype)

@@ -243,6 +243,26 @@ attn_status attn_fwd_kvcache_noalloc(const void *q, void *k_cache, void *v_cache
                                      attn_stream_t stream);
 
 /*
+ * FP8 forward (Inference Cookbook FAQ Q20: FP8 inside, BF16 out; FAQ Q10
+ * gives 1e-2 absolute / 1e-2 relative as the FP8 tolerance).  q (b,sq,hq,d)
+ * and k, v (b,sk,hkv,d) hold OCP FP8 E4M3 bytes; the inputs they stand for
+ * are q * descale_q, k * descale_k and v * descale_v (per-tensor factors,
+ * finite and > 0).  S = Q K^T runs on the tensor cores in FP8 with fp32
+ * accumulation; V is widened to bf16 into `workspace` (exactly) and P V runs
+ * in bf16.  out (b,sq,hq,d) is bf16 and lse (b,hq,sq) fp32, as attn_fwd.
+ * Masks, softcap, GQA as attn_fwd.  d must be 128 and sk > 0, else
+ * ATTN_ERR_UNSUPPORTED.  workspace: attn_fwd_fp8_workspace_size(...) bytes,
+ * 256-byte aligned.
+ */
+size_t attn_fwd_fp8_workspace_size(int b, int sk, int hkv, int d);
+
+attn_status attn_fwd_fp8(const void *q, const void *k, const void *v, void *out, float *lse,
+                         float descale_q, float descale_k, float descale_v, int b, int sq, int sk,
+                         int hq, int hkv, int d, float scale, int causal, int win_l, int win_r,
+                         float softcap, void *workspace, size_t workspace_bytes,
+                         attn_stream_t stream);
+
+/*
  * Debug only: the attention probabilities of a forward call (Inference
  * Cookbook FAQ Q9, return_attn_probs: the whole (batch, heads, seqlen_q,
  * seqlen_k) matrix costs O(N^2) memory, so it is for tests and debugging,

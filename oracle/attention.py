@@ -163,6 +163,17 @@ def probs(q, k, scale, causal=False, win_l=-1, win_r=-1, softcap=0.0):
     return p
 
 
+def fp8_forward(q8, k8, v8, descale_q, descale_k, descale_v, scale, causal=False, win_l=-1,
+                win_r=-1, softcap=0.0):
+    """FP8 forward (Inference Cookbook FAQ Q20: FP8 tensors stand for their
+    values times per-tensor descale factors; the output is BF16).  q8, k8, v8
+    are the E4M3 values widened to float64; the definition is the ordinary
+    forward of q8*descale_q, k8*descale_k, v8*descale_v.  Returns O, LSE
+    (float64; the library rounds O to bf16)."""
+    return forward(q8 * descale_q, k8 * descale_k, v8 * descale_v, scale, causal, win_l, win_r,
+                   softcap)
+
+
 def round_to(x, dtype):
     """Round float64 values to fp16 or bf16 (round to nearest even), as the
     forward's stored output is; returns float64."""

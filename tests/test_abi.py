@@ -123,3 +123,13 @@ def test_strided_argument_checks(lib):
     # PackGQA forced on needs hq / hkv to divide the 128-row tile
     assert lib.attn_fwd_strided(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 0, 0, 1, 1, 8, 8, 6, 2,
                                 128, 0.1, 0, -1, -1, 0.0, 1, None) == 2
+
+
+def test_fp8_host_checks(lib):
+    call = lambda dq=1.0, d=128, sk=8, ws=1 << 30: lib.attn_fwd_fp8(
+        FAKE, FAKE, FAKE, FAKE, FAKE, dq, 1.0, 1.0, 1, 8, sk, 4, 2, d, 0.1, 0, -1, -1, 0.0, FAKE,
+        ws, None)
+    assert call(dq=0.0) == 1 and call(dq=float("inf")) == 1
+    assert call(d=64) == 2 and call(sk=0) == 2
+    assert call(ws=16) == 3
+    assert lib.attn_fwd_fp8_workspace_size(2, 100, 8, 128) >= 2 * 100 * 8 * 128 * 2

@@ -441,3 +441,33 @@ def test_probability_matrix_reproduces_forward(kw):
     np.testing.assert_allclose(p.sum(axis=3)[:, :, nonempty], 1.0, atol=1e-12)
     assert np.all(p[:, :, ~nonempty] == 0.0)
     assert np.all(np.isneginf(lse[:, :, ~nonempty]))
+
+
+def test_e4m3_format_facts():
+    """OCP FP8 E4M3 (the format of FAQ Q20's FP8 tensors): bias 7, 3 mantissa
+    bits, no infinities; 0x38 = 1, 0x7E = 448 (largest), 0x08 = 2^-6 (smallest
+    normal), 0x01 = 2^-9 (smallest subnormal), 0x7F/0xFF = NaN."""
+    from exact_attention_41_gb300 import synthetic as syn
+
+    v = syn.e4m3_values()
+    assert v[0x38] == 1.0 and v[0xB8] == -1.0 and v[0x7E] == 448.0
+    assert v[0x08] == 2.0 ** -6 and v[0x01] == 2.0 ** -9 and v[0x00] == 0.0
+    assert np.isnan(v[0x7F]) and np.isnan(v[0xFF])
+    finite = np.flatnonzero(~np.isnan(v))
+    # every finite pattern survives a round trip (-0 keeps its sign bit)
+    assert np.array_equal(syn.round_e4m3(v[finite]), finite.astype(np.uint8))
+    # ties go to the even pattern, saturation at 448
+    assert syn.round_e4m3(np.array([1.0625, 1.1875, 1e6, -1e6])).tolist() == [0x38, 0x3A, 0x7E, 0xFE]
+
+
+def test_fp8_descale_placement():
+    """Only the product descale_q * descale_k * scale enters the scores, and
+    the output is linear in descale_v (FAQ Q20's descale of Q/K/V)."""
+    rng = np.random.default_rng(12)
+    q8, k8, v8 = (rng.standard_normal(sh) for sh in ((1, 6, 2, 8), (1, 9, 1, 8), (1, 9, 1, 8)))
+    o1, l1 = ref.fp8_forward(q8, k8, v8, 2.0, 0.25, 1.0, 0.3, causal=True)
+    o2, l2 = ref.fp8_forward(q8, k8, v8, 0.5, 1.0, 3.0, 0.3, causal=True)
+    np.testing.assert_allclose(3.0 * o1, o2, atol=1e-12)
+    np.testing.assert_allclose(l1, l2, atol=1e-12)
+    o3, _ = ref.forward(q8, k8, v8, 0.15, causal=True)
+    np.testing.assert_allclose(o1, o3, atol=1e-12)
