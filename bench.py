@@ -390,6 +390,19 @@ def run_ours(args, rank, world, local_rank):
     ms_bwd = timed(bwd, extra_steps, stream)
     ms_bwd_det = timed(lambda: bwd(True), extra_steps, stream)
 
+    # FP8 forward (E4M3 copies of q, k, v; descales 1): the S products on the
+    # FP8 tensor path, P V in bf16
+    q8, k8, v8 = (x.to(torch.float8_e4m3fn) for x in (q, k, v))
+    ws8 = torch.empty(libattn.lib().attn_fwd_fp8_workspace_size(B, S, HKV, D), device="cuda",
+                      dtype=torch.uint8)
+
+    def fwd8():
+        libattn.fwd_fp8(q8, k8, v8, causal=True, out=o, lse=lse, workspace=ws8)
+
+    fwd8()
+    ms_fwd8 = timed(fwd8, extra_steps, stream)
+    del q8, k8, v8, ws8
+
     # end to end through the public API from pinned host buffers
     hq_, hk_, hv_, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
     rq, rk, rv = (torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (dq, dk, dv))
@@ -430,6 +443,9 @@ def run_ours(args, rank, world, local_rank):
                     "frac": round(fwd_tflops / peak_t, 4)},
             "bwd": {"ms": round(ms_bwd, 4), "tflops": round(bwd_tflops, 2),
                     "frac": round(bwd_tflops / peak_t, 4)},
+            "fwd_fp8": {"ms": round(ms_fwd8, 4),
+                        "tflops": round(FWD_FLOPS / (ms_fwd8 * 1e-3) / 1e12, 2),
+                        "note": "E4M3 q,k,v; QK^T kind::f8f6f4, PV bf16; includes the V widening"},
             "bwd_deterministic": {"ms": round(ms_bwd_det, 4),
                                   "tflops": round(BWD_FLOPS / (ms_bwd_det * 1e-3) / 1e12, 2)},
             "roofline": {"bound": "tensor", "kernel": "backward (attn_bwd call)",
