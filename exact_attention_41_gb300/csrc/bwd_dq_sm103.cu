@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float s = __uint_as_float(su[col]);
           float p, dcap = 1.f;
           if (cap) {
-            const float tt = tanhf(s * cap_in);
+            const float tt = tanh_fast(s * cap_in);
             p = ex2(fmaf(f.softcap * kLog2e, tt, -lse2));
             dcap = 1.f - tt * tt;
           } else {

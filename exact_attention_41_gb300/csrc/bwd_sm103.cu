@@ -154,7 +154,7 @@ __device__ __forceinline__ void p_ds_16(const uint32_t *su, const uint32_t *du, 
         const float s = __uint_as_float(su[c]);
         float p, dcap = 1.f;
         if constexpr (kCap) {
-          const float t = tanhf(s * cap_in);
+          const float t = tanh_fast(s * cap_in);
           p = ex2(fmaf(cap_l2, t, -lv[2 * e2 + u]));
           dcap = 1.f - t * t;
         } else {

@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int q = 0; q < RP; ++q) {
         const float s = __uint_as_float(su[q]);
         const bool vis = key >= qlo[q] && key <= qhi[q];
-        x[q] = vis ? (cap ? cap_out * tanhf(s * cap_in) : s * sl2) : -INFINITY;
+        x[q] = vis ? (cap ? cap_out * tanh_fast(s * cap_in) : s * sl2) : -INFINITY;
         tmax[q] = x[q];
       }
       // column max over the 128 keys of the tile: warp shuffle, then across warps

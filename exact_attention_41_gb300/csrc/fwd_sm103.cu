@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
       // softcap, then the mask (Inference Cookbook FAQ Q22 order)
       if (cap) {
 #pragma unroll
-        for (int e = 0; e < BN; ++e) x[e] = cap_out * tanhf(x[e] * cap_in);
+        for (int e = 0; e < BN; ++e) x[e] = cap_out * tanh_fast(x[e] * cap_in);
       }
       const bool need_mask = key0 < lo_tile_max || key0 + BN - 1 > hi_tile_min;
       if (need_mask) {

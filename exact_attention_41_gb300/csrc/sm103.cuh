@@ -300,6 +300,20 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// tanh(x) = 1 - 2 / (exp(2x) + 1), from the definition of tanh, with the
+// hardware 2^x and reciprocal (ex2.approx / rcp.approx: relative errors
+// around 2^-22): two MUFU operations instead of a library call.  The result
+// has an absolute error of a few 1e-7 (the cancellation near x = 0 is in
+// absolute terms); for x -> +inf exp overflows to inf and the result is 1,
+// for x -> -inf it is -1.  Used for the softcap c * tanh(s / c), where
+// c * 1e-6 is far below the score's fp32 rounding at the sizes in use.
+__device__ __forceinline__ float tanh_fast(float x) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * 2.8853900817779268f));  // 2 log2(e)
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(e + 1.f));
+  return fmaf(-2.f, r, 1.f);
+}
+
 // Named barrier among `nthreads` threads (multiple of 32).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
