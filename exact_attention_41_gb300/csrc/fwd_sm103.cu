@@ -1,8 +1,12 @@
 // Forward attention on the 5th-generation tensor cores (sm_103a).
 //
-// One CTA owns one 128-row query tile of one (batch, head) and streams the
-// key/value tiles it may see ("FlashAttention完整说明" §二.1: tiling plus an
-// online softmax, so S and P never reach global memory).  Roles:
+// One CTA owns two 128-row query tiles (one for d = 256) of one (batch,
+// head) and streams the key/value tiles they may see ("FlashAttention完整说明"
+// §二.1: tiling plus an online softmax, so S and P never reach global
+// memory).  With PackGQA (Inference Cookbook FAQ Q15) a tile holds 128/g
+// query positions of all g query heads of one KV head instead.  The FP8
+// variant (QB = 1, FAQ Q20) reads E4M3 Q and K and computes S with
+// kind::f8f6f4; V is bf16 there too.  Roles:
 //
 //   warp 0      TMA producer: Q once, then K and V tiles into a smem ring.
 //   warp 1      MMA issuer (one elected lane): S_j = Q K_j^T into TMEM,
