@@ -133,3 +133,27 @@ def test_fp8_host_checks(lib):
     assert call(d=64) == 2 and call(sk=0) == 2
     assert call(ws=16) == 3
     assert lib.attn_fwd_fp8_workspace_size(2, 100, 8, 128) >= 2 * 100 * 8 * 128 * 2
+
+
+def test_split_heuristic_on_host(lib):
+    """Inference Cookbook FAQ Q14's split rules as implemented (host logic;
+    without a GPU the library assumes the GB300's 152 SMs): enough (batch, KV
+    head) units and short caches -> one split; long caches -> 8192-key pieces;
+    few units -> at least SMs / units splits, never more than 128-key tiles."""
+    if libattn_has_device():
+        pytest.skip("the SM count of the present GPU decides")
+    ns = lambda b, hkv, cap, n=0: lib.attn_kvcache_num_splits(b, 1, 32, hkv, 128, cap, n)
+    assert ns(64, 8, 4096) == 1
+    assert ns(64, 8, 33024) == 5
+    assert ns(1, 8, 4096) == 19          # ceil(152 / 8)
+    assert ns(1, 8, 1000) == 8           # capped by the 8 key tiles
+    assert ns(64, 8, 33024, 3) == 3      # explicit request wins
+
+
+def libattn_has_device():
+    try:
+        import torch
+
+        return torch.cuda.is_available()
+    except Exception:
+        return False
