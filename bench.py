@@ -409,12 +409,21 @@ def run_ours(args, rank, world, local_rank):
     h2d = sum(x.numel() * x.element_size() for x in (hq_, hk_, hv_, hdo))
     d2h = sum(x.numel() * x.element_size() for x in (rq, rk, rv))
 
+    # dO is first read by the backward, so its upload runs on a side stream
+    # while the forward computes (the step waits for it before the backward)
+    side = torch.cuda.Stream()
+
     def e2e_step():
+        main = torch.cuda.current_stream()
+        side.wait_stream(main)  # the previous step's backward is done with dO
+        with torch.cuda.stream(side):
+            do.copy_(hdo, non_blocking=True)
         q.copy_(hq_, non_blocking=True)
         k.copy_(hk_, non_blocking=True)
         v.copy_(hv_, non_blocking=True)
-        do.copy_(hdo, non_blocking=True)
-        step()
+        fwd()
+        main.wait_stream(side)
+        bwd()
         rq.copy_(dq, non_blocking=True)
         rk.copy_(dk, non_blocking=True)
         rv.copy_(dv, non_blocking=True)
