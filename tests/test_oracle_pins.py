@@ -471,3 +471,67 @@ def test_fp8_descale_placement():
     np.testing.assert_allclose(l1, l2, atol=1e-12)
     o3, _ = ref.forward(q8, k8, v8, 0.15, causal=True)
     np.testing.assert_allclose(o1, o3, atol=1e-12)
+
+
+@pytest.mark.parametrize("kw", [dict(causal=True), dict(win_l=3, win_r=2, softcap=2.5),
+                                dict(causal=True, win_l=4), dict()])
+@pytest.mark.parametrize("sq,sk", [(7, 7), (5, 11), (11, 5)])
+def test_forward_rows_is_dense_forward_at_samples(kw, sq, sk):
+    """forward_rows (the checker of the large-shape forward parity test) must
+    give exactly the dense forward's O[b, i, h] and LSE[b, h, i] for each
+    (b, h, i) sample: a wrong row offset under the bottom-right mask, a
+    swapped (b, h, i) order or a wrong GQA head would each fail here.  The
+    dense forward is pinned by the tests above."""
+    rng = np.random.default_rng(13)
+    b, hq, hkv, d = 2, 6, 2, 8
+    q = rng.standard_normal((b, sq, hq, d))
+    k, v = rng.standard_normal((b, sk, hkv, d)), rng.standard_normal((b, sk, hkv, d))
+    o, lse = ref.forward(q, k, v, 0.35, **kw)
+    samples = [(int(rng.integers(b)), int(rng.integers(hq)), int(rng.integers(sq)))
+               for _ in range(40)]
+    samples += [(0, 0, 0), (b - 1, hq - 1, sq - 1), (1, 3, sq // 2)]
+    ro, rl = ref.forward_rows(q, k, v, samples, 0.35, **kw)
+    for n, (bi, h, i) in enumerate(samples):
+        np.testing.assert_allclose(ro[n], o[bi, i, h], rtol=1e-13, atol=1e-14)
+        if np.isneginf(lse[bi, h, i]):
+            assert np.isneginf(rl[n])
+        else:
+            np.testing.assert_allclose(rl[n], lse[bi, h, i], rtol=1e-13, atol=1e-14)
+
+
+@pytest.mark.parametrize("softcap", [0.0, 3.0])
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_stored_output_reading_closed_form(softcap, dt):
+    """The stored-output reading of D against an independent closed form.
+    With delta_i = dO_i . (O_i - round(O_i)) (O the exact output, round the
+    storage rounding), using the stored O in D changes dS by P_ij delta_i, so
+    the gradients move by exactly the gradient of sum_i delta_i LSE_i:
+        dQ_stored - dQ_exact = d/dQ sum_i delta_i LSE_i,  same for dK,
+        dV_stored = dV_exact.
+    Everything on the right is computed with torch float64 autograd and
+    torch's own fp16/bf16 rounding, not with the oracle."""
+    torch = pytest.importorskip("torch")
+    b, s, hq, hkv, d, scale = 1, 13, 4, 2, 8, 0.45
+    q, k, v, do = rnd(66, b, s, hq, d), rnd(67, b, s, hkv, d), rnd(68, b, s, hkv, d), rnd(69, b, s, hq, d)
+    g = hq // hkv
+    tq = torch.tensor(q.transpose(0, 2, 1, 3), requires_grad=True)
+    tk = torch.tensor(np.repeat(k, g, axis=2).transpose(0, 2, 1, 3), requires_grad=True)
+    tv = torch.tensor(np.repeat(v, g, axis=2).transpose(0, 2, 1, 3))
+    s_ = scale * tq @ tk.transpose(-1, -2)
+    if softcap:
+        s_ = softcap * torch.tanh(s_ / softcap)
+    s_ = s_.masked_fill(~torch.ones(s, s, dtype=torch.bool).tril(), float("-inf"))
+    lse = torch.logsumexp(s_, dim=-1)
+    with torch.no_grad():
+        o = torch.softmax(s_, dim=-1) @ tv
+        o_r = o.to(torch.bfloat16 if dt == "bf16" else torch.float16).to(torch.float64)
+        delta = (torch.tensor(do.transpose(0, 2, 1, 3)) * (o - o_r)).sum(-1)
+    (lse * delta).sum().backward()
+    corr_q = tq.grad.numpy().transpose(0, 2, 1, 3)
+    corr_k = tk.grad.numpy().transpose(0, 2, 1, 3).reshape(b, s, hkv, g, d).sum(3)
+    exact = ref.backward(q, k, v, do, scale, causal=True, softcap=softcap)
+    got = ref.backward(q, k, v, do, scale, causal=True, softcap=softcap, stored_o=dt)
+    assert np.abs(corr_q).max() > 0
+    np.testing.assert_allclose(got[0] - exact[0], corr_q, rtol=1e-9, atol=1e-13)
+    np.testing.assert_allclose(got[1] - exact[1], corr_k, rtol=1e-9, atol=1e-13)
+    np.testing.assert_array_equal(got[2], exact[2])
