@@ -13,6 +13,7 @@ decode workload (HBM GB/s), an end-to-end pass through the public API from
 pinned host buffers, and the float64 CPU oracle on a bounded sample.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+       python bench.py --profile-case fwd|bwd|decode   (one small case for ncu)
 Under torchrun each rank runs its own replica (weak scaling) and rank 0
 prints one JSON line.
 """
@@ -283,11 +284,175 @@ def cpu_baseline_sample(repeat=1):
         ref.head_backward(q, k, v, do, S, S, 1 / math.sqrt(D), causal=True)
     dt = (time.perf_counter() - t0) / repeat
     flops = STEP_FLOPS / (B * HQ)
+    n1 = 4096
+    t1 = one_thread_seconds(n1)
+    flops1 = 3.5 * 4 * n1 * n1 * D / 2
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
             "kind": "oracle",
             "sample": "float64 oracle fwd+bwd of one (batch, head) of the training shape "
                       f"(s=8192, d=128, causal), {dt:.2f} s; algorithmic causal FLOPs "
-                      f"{flops:.3e}; numpy/BLAS on all host threads"}
+                      f"{flops:.3e}; numpy/BLAS on all host threads",
+            "one_thread": None if t1 is None else {
+                "value": round(flops1 / t1 / 1e12, 6), "unit": "TFLOP/s", "seconds": round(t1, 2),
+                "sample": f"the same on the causal prefix of {n1} tokens, one BLAS thread"},
+            "cpu": cpu_info()}
+
+
+def bench_e2e(libattn, inputs, fwd_bwd_into, steps, stream):
+    """The training step through the public API with the data on the host:
+    every step uploads its q, k, v, dO from pinned host memory and reads its
+    dq, dk, dv back into pinned host memory.  Device buffers are doubled so
+    that the uploads of step i+1 and the downloads of step i-1 run on two copy
+    streams while step i computes; the first upload and the last download are
+    inside the timed region too.  Afterwards the downloaded gradients are
+    compared with an eager step on the same inputs."""
+    import torch
+
+    host_in = [x.cpu().pin_memory() for x in inputs]
+    bufs = [[torch.empty_like(x) for x in inputs] for _ in range(2)]
+    grads = [[torch.empty_like(x) for x in inputs[:3]] for _ in range(2)]
+    host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in inputs[:3]]
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
+    ev = lambda: torch.cuda.Event()
+    up_done, comp_done, down_done = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+
+    def run(n):
+        main = torch.cuda.current_stream()
+        up.wait_stream(main)
+        down.wait_stream(main)
+        for i in range(n):
+            s = i % 2
+            with torch.cuda.stream(up):
+                if i >= 2:
+                    up.wait_event(comp_done[s])  # step i-2 no longer reads set s
+                for d, h in zip(bufs[s], host_in):
+                    d.copy_(h, non_blocking=True)
+                up_done[s].record(up)
+            main.wait_event(up_done[s])
+            if i >= 2:
+                main.wait_event(down_done[s])    # step i-2's gradients are read out
+            fwd_bwd_into(*bufs[s], *grads[s])
+            comp_done[s].record(main)
+            with torch.cuda.stream(down):
+                down.wait_event(comp_done[s])
+                for h, d in zip(host_out, grads[s]):
+                    h.copy_(d, non_blocking=True)
+                down_done[s].record(down)
+        main.wait_stream(up)
+        main.wait_stream(down)
+
+    run(2)
+    ms = timed(lambda: run(steps), 1, stream) / steps
+    torch.cuda.synchronize()
+    # the last step's downloaded gradients against an eager step
+    ref = [torch.empty_like(x) for x in inputs[:3]]
+    fwd_bwd_into(*inputs, *ref)
+    torch.cuda.synchronize()
+    same_kv = all(torch.equal(h.cuda().view(torch.int16), r.view(torch.int16))
+                  for h, r in zip(host_out[1:], ref[1:]))
+    dq_ok = torch.allclose(host_out[0].cuda().float(), ref[0].float(), atol=1e-2, rtol=1e-2)
+    info = {"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "overlap": "double-buffered device inputs/gradients; uploads and downloads on two "
+                       "copy streams overlap the neighbouring steps' compute",
+            "check": {"dk_dv_bitwise_equal_to_eager": bool(same_kv),
+                      "dq_within_1e-2_of_eager": bool(dq_ok)}}
+    del host_in, bufs, grads, host_out
+    return ms, info
+
+
+def accuracy_sample(libattn, inputs, o, lse, ws):
+    """Error of the training step against the float64 oracle on one (batch,
+    KV head) group -- the forward output and the gradients, against the
+    oracle's stored-O reading of D and against the exact gradient -- as the
+    worst error/bound ratio and the fraction out of bound for the contract
+    (bf16: 1e-2 + 1e-2 |ref|) and for the Inference Cookbook FAQ Q10 bf16
+    tolerance (5e-3 + 5e-3 |ref|).  Reported, not asserted."""
+    import numpy as np
+    import torch
+
+    from oracle import attention as ref
+
+    q, k, v, do = inputs
+    dq, dk, dv = (torch.empty_like(x) for x in (q, k, v))
+    libattn.fwd(q, k, v, causal=True, out=o, lse=lse)
+    libattn.bwd(q, k, v, o, lse, do, causal=True, workspace=ws, dq=dq, dk=dk, dv=dv)
+    torch.cuda.synchronize()
+    bi, kv, g = 1, 3, HQ // HKV
+    hs = slice(kv * g, (kv + 1) * g)
+    t0 = time.perf_counter()
+    f64 = lambda t: t.double().cpu().numpy()
+    qg, dog = f64(q[bi:bi + 1, :, hs]), f64(do[bi:bi + 1, :, hs])
+    kg, vg = f64(k[bi:bi + 1, :, kv:kv + 1]), f64(v[bi:bi + 1, :, kv:kv + 1])
+    scale = 1 / math.sqrt(D)
+    ro, _ = ref.forward(qg, kg, vg, scale, causal=True)
+    stored = ref.backward(qg, kg, vg, dog, scale, causal=True, stored_o="bf16")
+    exact = ref.backward(qg, kg, vg, dog, scale, causal=True)
+    got = {"O": f64(o[bi:bi + 1, :, hs]), "dQ": f64(dq[bi:bi + 1, :, hs]),
+           "dK": f64(dk[bi:bi + 1, :, kv:kv + 1]), "dV": f64(dv[bi:bi + 1, :, kv:kv + 1])}
+
+    def stats(x, r):
+        err = np.abs(x - r)
+        res = {"max_abs_err": float(err.max())}
+        for name, tol in (("contract", 1e-2), ("pages_q10", 5e-3)):
+            bound = tol + tol * np.abs(r)
+            res[name] = {"worst_ratio": round(float((err / bound).max()), 4),
+                         "frac_out": float((err > bound).mean())}
+        return res
+
+    res = {"sample": f"batch {bi}, kv head {kv} (query heads {hs.start}-{hs.stop - 1}) of the "
+                     "training step, all 8192 rows, atomic dQ",
+           "O": stats(got["O"], ro)}
+    for n, i in (("dQ", 0), ("dK", 1), ("dV", 2)):
+        res[n + "_vs_stored_o"] = stats(got[n], stored[i])
+        res[n + "_vs_exact"] = stats(got[n], exact[i])
+    res["oracle_seconds"] = round(time.perf_counter() - t0, 1)
+    return res
+
+
+def cpu_info():
+    """Host CPU model, architecture and thread count (for the baseline)."""
+    import platform
+
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"model": model, "arch": platform.machine(), "nproc": os.cpu_count()}
+
+
+ONE_THREAD_SNIPPET = """
+import math, sys, time
+import numpy as np
+sys.path.insert(0, {root!r})
+from exact_attention_41_gb300 import synthetic as syn
+from oracle import attention as ref
+n, d = {n}, {d}
+rng = np.random.default_rng(90)
+q, k, v, do = (syn.bits_to_f64(syn.normal_bits(rng, (n, d), syn.BF16), syn.BF16) for _ in range(4))
+t0 = time.perf_counter()
+ref.head_forward(q, k, v, np.arange(n), n, n, 1 / math.sqrt(d), causal=True)
+ref.head_backward(q, k, v, do, n, n, 1 / math.sqrt(d), causal=True)
+print(time.perf_counter() - t0)
+"""
+
+
+def one_thread_seconds(n):
+    """The oracle's fwd+bwd of one (batch, head) causal prefix of n tokens in
+    a child process limited to one BLAS/OpenMP thread; None if it fails."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    try:
+        r = subprocess.run([sys.executable, "-c", ONE_THREAD_SNIPPET.format(root=ROOT, n=n, d=D)],
+                           capture_output=True, text=True, env=env, timeout=300)
+        return float(r.stdout.strip().splitlines()[-1])
+    except (OSError, subprocess.SubprocessError, ValueError, IndexError):
+        return None
 
 
 # ------------------------------------------------------------------ arms
@@ -373,6 +538,10 @@ def run_ours(args, rank, world, local_rank):
         fwd()
         bwd()
 
+    def fwd_bwd_into(xq, xk, xv, xdo, gq, gk, gv):
+        libattn.fwd(xq, xk, xv, causal=True, out=o, lse=lse)
+        libattn.bwd(xq, xk, xv, o, lse, xdo, causal=True, workspace=ws, dq=gq, dk=gk, dv=gv)
+
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
@@ -404,33 +573,7 @@ def run_ours(args, rank, world, local_rank):
     del q8, k8, v8, ws8
 
     # end to end through the public API from pinned host buffers
-    hq_, hk_, hv_, hdo = (x.cpu().pin_memory() for x in (q, k, v, do))
-    rq, rk, rv = (torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (dq, dk, dv))
-    h2d = sum(x.numel() * x.element_size() for x in (hq_, hk_, hv_, hdo))
-    d2h = sum(x.numel() * x.element_size() for x in (rq, rk, rv))
-
-    # dO is first read by the backward, so its upload runs on a side stream
-    # while the forward computes (the step waits for it before the backward)
-    side = torch.cuda.Stream()
-
-    def e2e_step():
-        main = torch.cuda.current_stream()
-        side.wait_stream(main)  # the previous step's backward is done with dO
-        with torch.cuda.stream(side):
-            do.copy_(hdo, non_blocking=True)
-        q.copy_(hq_, non_blocking=True)
-        k.copy_(hk_, non_blocking=True)
-        v.copy_(hv_, non_blocking=True)
-        fwd()
-        main.wait_stream(side)
-        bwd()
-        rq.copy_(dq, non_blocking=True)
-        rk.copy_(dk, non_blocking=True)
-        rv.copy_(dv, non_blocking=True)
-
-    e2e_step()
-    ms_e2e = timed(e2e_step, extra_steps, stream)
-
+    ms_e2e, e2e_info = bench_e2e(libattn, (q, k, v, do), fwd_bwd_into, extra_steps, stream)
     out = None
     if rank == 0:
         peak_t = pk["bf16_tflops"]
@@ -467,12 +610,13 @@ def run_ours(args, rank, world, local_rank):
                              "achieved": round(fwd_tflops, 2), "peak": peak_t, "unit": "TFLOP/s",
                              "frac": round(fwd_tflops / peak_t, 4), "traffic": traffic_for("fwd")},
             "e2e": {"value": round(world * STEP_FLOPS / (ms_e2e * 1e-3) / 1e12, 2),
-                    "unit": "TFLOP/s", "ms_per_step": round(ms_e2e, 4),
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                    "unit": "TFLOP/s", "ms_per_step": round(ms_e2e, 4), **e2e_info},
             "gpu_launches": launches,
             "clocks": clk.summary(),
         }
-    del hq_, hk_, hv_, hdo, rq, rk, rv, ws_det
+    del ws_det
+    if rank == 0 and not args.no_accuracy:
+        out["accuracy"] = accuracy_sample(libattn, (q, k, v, do), o, lse, ws)
     if rank == 0 and not args.no_extras:
         del q, k, v, do, o, lse, dq, dk, dv, ws
         torch.cuda.empty_cache()
@@ -492,6 +636,54 @@ def run_ours(args, rank, world, local_rank):
         dist.destroy_process_group()
 
 
+def run_profile_case(args):
+    """One small, fixed case of one kernel family, for profiler captures
+    (no timing, no JSON line): `--profile-case fwd|bwd` runs the causal
+    bf16 b=1 s=8192 hq=32 hkv=8 d=128 problem (`--deterministic` for that
+    backward mode), `decode` the paged decode of b=8, sq=s_new=4, hq=32 (the
+    workload's heads), caches U[1,32768] -- each larger than L2 in its K/V or
+    Q/dO streams and about 1 GB on the device at most.  `--calls` calls (a
+    warm-up and the one to capture), then the device error word is checked."""
+    import torch
+
+    from exact_attention_41_gb300 import build as build_mod
+
+    build_mod.build()
+    from exact_attention_41_gb300 import libattn
+    from exact_attention_41_gb300 import synthetic as syn
+
+    bf = syn.BF16
+    if args.profile_case in ("fwd", "bwd"):
+        b, s, hq, hkv = 1, S, HQ, HKV
+        q = syn.device_normal((b, s, hq, D), bf, 1)
+        k = syn.device_normal((b, s, hkv, D), bf, 2)
+        v = syn.device_normal((b, s, hkv, D), bf, 3)
+        if args.profile_case == "fwd":
+            for _ in range(args.calls):
+                libattn.fwd(q, k, v, causal=True)
+        else:
+            do = syn.device_normal((b, s, hq, D), bf, 4)
+            o, lse = libattn.fwd(q, k, v, causal=True)
+            for _ in range(args.calls):
+                libattn.bwd(q, k, v, o, lse, do, causal=True, deterministic=args.deterministic)
+    else:
+        b, sq, page = 8, 4, 256
+        seqlens, table, npages = syn.decode_layout(9, b, 32768, page, sq)
+        kc = syn.device_normal((npages, page, HKV, D), bf, 5)
+        vc = syn.device_normal((npages, page, HKV, D), bf, 6)
+        q = syn.device_normal((b, sq, HQ, D), bf, 7)
+        kn = syn.device_normal((b, sq, HKV, D), bf, 8)
+        vn = syn.device_normal((b, sq, HKV, D), bf, 9)
+        sl = torch.from_numpy(seqlens).cuda()
+        bt = torch.from_numpy(table).cuda()
+        for _ in range(args.calls):
+            libattn.fwd_kvcache(q, kc, vc, sl, k_new=kn, v_new=vn, block_table=bt, causal=True)
+    torch.cuda.synchronize()
+    st = libattn.device_error()
+    print("profile case", args.profile_case, "done; device error", st, flush=True)
+    sys.exit(0 if st == (0, 0) else 1)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -500,10 +692,18 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-extras", action="store_true", help="skip varlen/decode lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-accuracy", action="store_true", help="skip the oracle error sample")
+    ap.add_argument("--profile-case", choices=["fwd", "bwd", "decode"],
+                    help="run one small fixed case for a profiler capture and exit")
+    ap.add_argument("--calls", type=int, default=2, help="calls of --profile-case")
+    ap.add_argument("--deterministic", action="store_true", help="--profile-case bwd mode")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.profile_case:
+        run_profile_case(args)
+        return
     if args.impl == "reference":
         run_reference(args, rank)
         return

@@ -1,6 +1,9 @@
 // The libattn C ABI: argument validation, workspace sizing and dispatch.
 // Declarations and the contract of every entry point are in include/libattn.h.
 #include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
 
 #include <atomic>
 #include <mutex>
@@ -12,6 +15,17 @@ namespace {
 
 // Sticky device error word, one per device that loads the library.
 __device__ int g_device_error;
+
+// Wall-clock limit of one device-side wait, read by every call
+// (attn_set_wait_limit_ns).
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // 2 s
+std::atomic<unsigned long long> g_wait_ns{kDefaultWaitNs};
+
+uint64_t wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
+// attn_set_test_stall: read by every call into its kernel arguments.
+std::atomic<int> g_test_stall{0};
+int test_stall() { return g_test_stall.load(std::memory_order_relaxed); }
 
 constexpr int kMaxDevices = 64;
 
@@ -90,11 +104,11 @@ int resolve_pack(int pack_gqa, int hq, int hkv, int max_sq) {
 
 attn_status launched(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
-// Backward workspace for `rows` query rows in total: D_i (fp32, LSE
-// layout) and, unless deterministic, the fp32 dQ accumulator of the
-// key-stationary kernel's atomic adds.
+// Backward workspace for `rows` query rows in total: D_i and -LSE_i log2(e)
+// (fp32, LSE layout each) and, unless deterministic, the fp32 dQ
+// accumulator of the key-stationary kernel's atomic adds.
 size_t bwd_ws_bytes(int64_t rows, int hq, int d, int deterministic) {
-  return align256(sizeof(float2) * rows * hq) +
+  return 2 * align256(sizeof(float) * rows * hq) +
          (deterministic ? 0 : align256(sizeof(float) * rows * hq * d));
 }
 
@@ -103,10 +117,13 @@ attn_status run_bwd(BwdArgs &a, int64_t rows, void *workspace, const DeviceInfo 
                     cudaStream_t stream) {
   char *ws = static_cast<char *>(workspace);
   const int hq = a.f.hq;
-  a.dsum = reinterpret_cast<float *>(ws);   // one of the two, by path
-  a.lsd = reinterpret_cast<float2 *>(ws);
-  ws += align256(sizeof(float2) * rows * hq);
+  a.dsum = reinterpret_cast<float *>(ws);
+  ws += align256(sizeof(float) * rows * hq);
+  a.nlse2 = reinterpret_cast<float *>(ws);
+  ws += align256(sizeof(float) * rows * hq);
   a.dq_acc = a.deterministic ? nullptr : reinterpret_cast<float *>(ws);
+  a.f.wait_ns = wait_limit_ns();
+  a.f.stall = test_stall();
   if (a.f.d == 128) return launched(launch_bwd_tc(a, di->sms, stream));
   return launched(launch_bwd_simt(a, stream));
 }
@@ -132,6 +149,24 @@ std::atomic<unsigned long long> g_launches{0};
 }  // namespace
 
 void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+bool debug_enabled() {
+  static const bool on = [] {
+    const char *e = getenv("LIBATTN_DEBUG");
+    return e != nullptr && atoi(e) != 0;
+  }();
+  return on;
+}
+
+void debug_log(const char *fmt, ...) {
+  if (!debug_enabled()) return;
+  char line[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(line, sizeof line, fmt, ap);
+  va_end(ap);
+  fprintf(stderr, "libattn: %s\n", line);
+}
 
 }  // namespace attn
 
@@ -178,6 +213,8 @@ attn_status attn_fwd_strided(const void *q, const void *k, const void *v, void *
   FwdArgs a{q, k, v, out, lse, Seqs{nullptr, nullptr, sq, sk, 0, 0, hq}, b, hq, hkv, d, dtype,
             scale, softcap > 0.f ? softcap : 0.f, win_l, win_r, di->err};
   set_strides(a, q_row_stride, k_row_stride, v_row_stride);
+  a.wait_ns = wait_limit_ns();
+  a.stall = test_stall();
   a.pack = pack;
   return launched(launch_fwd_tc(a, stream));
 }
@@ -225,7 +262,8 @@ attn_status attn_bwd_strided(const void *q, const void *k, const void *v, const 
   BwdArgs a{FwdArgs{q, k, v, const_cast<void *>(out), const_cast<float *>(lse),
                     Seqs{nullptr, nullptr, sq, sk, 0, 0, hq}, b, hq, hkv, d, dtype, scale,
                     softcap > 0.f ? softcap : 0.f, win_l, win_r, di->err},
-            dout, dq, dk, dv, nullptr, nullptr, nullptr, deterministic};
+            dout, dq, dk, dv};
+  a.deterministic = deterministic;
   set_strides(a.f, q_row_stride, k_row_stride, v_row_stride);
   set_grad_strides(a, dq_row_stride, dk_row_stride, dv_row_stride);
   return run_bwd(a, (int64_t)b * sq, workspace, di, stream);
@@ -265,6 +303,8 @@ attn_status attn_fwd_varlen(const void *q, const void *k, const void *v, void *o
             batch, hq, hkv, d, dtype, scale, softcap > 0.f ? softcap : 0.f, win_l, win_r,
             di->err};
   set_strides(a, 0, 0, 0);
+  a.wait_ns = wait_limit_ns();
+  a.stall = test_stall();
   a.pack = resolve_pack(-1, hq, hkv, max_seqlen_q);
   return launched(launch_fwd_tc(a, stream));
 }
@@ -307,7 +347,8 @@ attn_status attn_bwd_varlen(const void *q, const void *k, const void *v, const v
                     Seqs{cu_seqlens_q, cu_seqlens_k, max_seqlen_q, max_seqlen_k, total_q, total_k, hq},
                     batch, hq, hkv, d, dtype, scale, softcap > 0.f ? softcap : 0.f, win_l, win_r,
                     di->err},
-            dout, dq, dk, dv, nullptr, nullptr, nullptr, deterministic};
+            dout, dq, dk, dv};
+  a.deterministic = deterministic;
   set_strides(a.f, 0, 0, 0);
   set_grad_strides(a, 0, 0, 0);
   return run_bwd(a, total_q, workspace, di, stream);
@@ -372,6 +413,8 @@ attn_status attn_fwd_kvcache(const void *q, void *k_cache, void *v_cache, const 
                                 ws + align256(sizeof(float) * (size_t)splits * b * sq * hq * d))
                           : nullptr,
                di->err};
+  a.wait_ns = wait_limit_ns();
+  a.stall = test_stall();
   return launched(launch_decode(a, stream));
 }
 
@@ -392,6 +435,8 @@ attn_status attn_fwd_probs(const void *q, const void *k, const float *lse, float
             Seqs{nullptr, nullptr, sq, sk, 0, 0, hq}, b, hq, hkv, d, dtype, scale,
             softcap > 0.f ? softcap : 0.f, win_l, win_r, di->err};
   set_strides(a, 0, 0, 0);
+  a.wait_ns = wait_limit_ns();
+  a.stall = test_stall();
   return launched(launch_probs(a, p, stream));
 }
 
@@ -429,6 +474,8 @@ attn_status attn_fwd_fp8(const void *q, const void *k, const void *v, void *out,
   FwdArgs a{q, k, workspace, out, lse, Seqs{nullptr, nullptr, sq, sk, 0, 0, hq}, b, hq, hkv, d,
             ATTN_BF16, eff, softcap > 0.f ? softcap : 0.f, win_l, win_r, di->err};
   set_strides(a, 0, 0, 0);
+  a.wait_ns = wait_limit_ns();
+  a.stall = test_stall();
   a.pack = resolve_pack(-1, hq, hkv, sq);
   a.qk_fp8 = 1;
   a.out_scale = descale_v;
@@ -443,6 +490,12 @@ attn_status attn_kvcache_advance(int32_t *cache_seqlens, int b, int s_new, attn_
 }
 
 unsigned long long attn_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+unsigned long long attn_set_wait_limit_ns(unsigned long long ns) {
+  return g_wait_ns.exchange(ns == 0 ? kDefaultWaitNs : ns, std::memory_order_relaxed);
+}
+
+int attn_set_test_stall(int on) { return g_test_stall.exchange(on != 0, std::memory_order_relaxed); }
 
 attn_status attn_get_device_error(attn_stream_t stream, int *detail) {
   const DeviceInfo *di = device_info();

@@ -5,8 +5,9 @@
 // column slices of the head dimension for the accumulations, exchanging the
 // per-key scalars with warp shuffles.  The forward is the online softmax of
 // "FlashAttention完整说明" §二.1 with key blocks of 32; the backward
-// recomputes P from Q, K and the saved LSE (§二.2).  Used for the varlen
-// problems and as the general-shape path.
+// recomputes P from Q, K and the saved LSE (§二.2).  Used where the
+// tensor-core kernels do not apply: the backward for d = 64 and d = 256, and
+// the forward of a problem with no keys at all.
 #include "kernels.h"
 
 namespace attn {
@@ -250,6 +251,7 @@ cudaError_t bwd_rows(const BwdArgs &a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t st) {
+  debug_log("forward: row kernel on CUDA cores (one warp per query row), d=%d", a.d);
   const bool bf = a.dtype == ATTN_BF16;
   switch (a.d) {
     case 64: return bf ? fwd_rows<__nv_bfloat16, 64>(a, st) : fwd_rows<__half, 64>(a, st);
@@ -260,6 +262,7 @@ cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t st) {
 }
 
 cudaError_t launch_bwd_simt(const BwdArgs &a, cudaStream_t st) {
+  debug_log("backward: row kernels on CUDA cores (one warp per query / key row), d=%d", a.f.d);
   const bool bf = a.f.dtype == ATTN_BF16;
   switch (a.f.d) {
     case 64: return bf ? bwd_rows<__nv_bfloat16, 64>(a, st) : bwd_rows<__half, 64>(a, st);

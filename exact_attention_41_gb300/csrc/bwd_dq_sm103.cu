@@ -41,6 +41,8 @@ struct Shared {
   uint64_t q_full;
   uint64_t kv_full[ST], kv_empty[ST];
   uint64_t s_full[NT], ds_full[NT], dq_done[NT];
+  uint64_t all_done;  // every MMA of the CTA has completed
+  uint64_t wait_ns;   // wall-clock limit of a wait
   uint32_t tmem_base;
   int abort;
 };
@@ -52,7 +54,7 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 __device__ __forceinline__ bool wait_bar(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
-  return mbar_wait_bounded(smem_u32(bar), parity, &sh.abort, err);
+  return mbar_wait_bounded(smem_u32(bar), parity, &sh.abort, err, sh.wait_ns);
 }
 
 __device__ __forceinline__ bool wait_warp(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
@@ -109,6 +111,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.ds_full[t], BM);
       mbar_init(&sh.dq_done[t], 1);
     }
+    mbar_init(&sh.all_done, 1);
+    sh.wait_ns = f.wait_ns;
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -187,8 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                    desc_add(k_mn, ko + kk * 16 * 128), id_q, (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&sh.dq_done[t]);
         };
-        bool ok = wait_bar(sh, &sh.q_full, 0, f.err) &&
-                  wait_bar(sh, &sh.kv_full[0], 0, f.err);
+        // test hook: all_done completes only after this thread's last
+        // commit, so this wait can only run out
+        bool ok = !(f.stall && !wait_bar(sh, &sh.all_done, 0, f.err));
+        ok = ok && wait_bar(sh, &sh.q_full, 0, f.err) && wait_bar(sh, &sh.kv_full[0], 0, f.err);
         tc_fence_after();
         if (ok)
           for (int t = 0; t < NT; ++t) mma_sdp(t, 0);
@@ -211,6 +217,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        // after an abort, no MMA may still run when the TMEM is released
+        mma_commit(&sh.all_done);
+        if (*(volatile int *)&sh.abort) {
+          int *noerr = nullptr;
+          mbar_wait(&sh.all_done, 0, noerr);
+        }
       }
     }
   } else {
@@ -227,8 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     key_range(m0 + t * BM, lq, lk, f.win_l, f.win_r, dummy, hi_tile_min);
     const bool valid = i < lq;
     const int64_t li = f.seqs.lse_index(b, h, q0, valid ? i : 0);
-    const float2 ld = valid ? a.lsd[li] : make_float2(0.f, 0.f);  // (LSE * log2(e), D)
-    const float lse2 = ld.x, dsum = ld.y;
+    const float nlse2 = valid ? a.nlse2[li] : 0.f;  // -LSE * log2(e)
+    const float dsum = valid ? a.dsum[li] : 0.f;
     const bool cap = f.softcap > 0.f;
     const float sl2 = f.scale * kLog2e, cap_in = cap ? f.scale / f.softcap : 0.f;
     bool ok = true;
@@ -254,10 +266,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           float p, dcap = 1.f;
           if (cap) {
             const float tt = tanh_fast(s * cap_in);
-            p = ex2(fmaf(f.softcap * kLog2e, tt, -lse2));
+            p = ex2(fmaf(f.softcap * kLog2e, tt, nlse2));
             dcap = 1.f - tt * tt;
           } else {
-            p = ex2(fmaf(s, sl2, -lse2));
+            p = ex2(fmaf(s, sl2, nlse2));
           }
           if (need_mask) {
             const int kj = key0 + col;
@@ -328,6 +340,9 @@ cudaError_t bwd_dq(const BwdArgs &a, cudaStream_t st) {
   const int64_t grid = (int64_t)m_blocks * f.hq * f.batch;
   if (grid == 0) return cudaSuccess;
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
+  debug_log("backward dQ (deterministic): bwd_dq_kernel d=128, %d query tiles of %d rows per "
+            "CTA, %d-key tiles, grid=%lld CTAs x %d threads, smem=%d B", NT, BM, BN,
+            (long long)grid, kThreads, kSmem);
   bwd_dq_kernel<T><<<(unsigned)grid, kThreads, kSmem, st>>>(tq, tk, tv, tdo, a, m_blocks);
   count_launches(1);
   return cudaGetLastError();

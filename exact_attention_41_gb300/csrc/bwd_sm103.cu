@@ -68,10 +68,13 @@ struct Shared {
   uint64_t pds_full[2];  // its P^T (TMEM) and dS^T (shared memory) are written
   uint64_t dq_full[2], dq_free[2];
   uint64_t all_done;     // every MMA of the CTA has completed
+  uint64_t wait_ns;      // wall-clock limit of a wait
   uint32_t tmem_base;
   int abort;
-  // (LSE * log2(e), D) of each ring stage's 64 queries, copied with the stage
-  alignas(16) float2 lsd[ST][BQ];
+  // -LSE * log2(e) and D of each ring stage's 64 queries, copied with the
+  // stage; per pair of queries (2p, 2p+1): {-LSE_2p, -LSE_2p+1, D_2p, D_2p+1}
+  // (log2 units), so a 16-byte load gives both packed pairs
+  alignas(16) float lsd[ST][2 * BQ];
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -81,7 +84,7 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 __device__ __forceinline__ bool wait_bar(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
-  return mbar_wait_bounded(smem_u32(bar), parity, &sh.abort, err);
+  return mbar_wait_bounded(smem_u32(bar), parity, &sh.abort, err, sh.wait_ns);
 }
 
 // The same wait taken by a whole warp with one answer, so warp-collective
@@ -98,21 +101,27 @@ __device__ __forceinline__ void red_add(float *p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
-// x = hi + lo with hi, lo 16-bit: packed pairs of the high parts and of the
-// low parts.  bf16: hi is x with its low 16 bits cleared (truncation), so
-// lo = x - hi is exact in fp32 and only lo is rounded; fp16: hi rounded to
-// nearest, lo the rounded remainder.
+// x = hi + lo with hi, lo 16-bit, for the two values of a packed pair: hi
+// and lo are the packed 16-bit pairs.  bf16: hi is x with its low 16 bits
+// cleared (truncation), so lo = x - hi is exact in fp32 and only lo is
+// rounded; fp16: hi rounded to nearest, lo the rounded remainder.
 template <typename T>
-__device__ __forceinline__ void split_hi_lo(const float (&x)[2], uint32_t &hi, uint32_t &lo) {
+__device__ __forceinline__ void split_hi_lo(uint64_t x2, uint32_t &hi, uint32_t &lo) {
+  float x0, x1;
+  f2_unpack(x2, x0, x1);
+  uint64_t h2;
   if constexpr (IsBf16<T>::v) {
-    const uint32_t a = __float_as_uint(x[0]) & 0xFFFF0000u, b = __float_as_uint(x[1]) & 0xFFFF0000u;
+    const uint32_t a = __float_as_uint(x0), b = __float_as_uint(x1);
     hi = __byte_perm(a, b, 0x7632);  // high halves of a and b -> (a, b) packed
-    lo = Elem<T>::from_f2(x[0] - __uint_as_float(a), x[1] - __uint_as_float(b));
+    h2 = f2_pack(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(b & 0xFFFF0000u));
   } else {
-    hi = Elem<T>::from_f2(x[0], x[1]);
+    hi = Elem<T>::from_f2(x0, x1);
     const float2 h = Elem<T>::to_f2(hi);
-    lo = Elem<T>::from_f2(x[0] - h.x, x[1] - h.y);
+    h2 = f2_pack(h.x, h.y);
   }
+  float l0, l1;
+  f2_unpack(f2_sub(x2, h2), l0, l1);
+  lo = Elem<T>::from_f2(l0, l1);
 }
 
 // Query chunks [c_lo, c_lo + nch) that can see any key of block nb.
@@ -132,42 +141,43 @@ __device__ __forceinline__ void chunk_range(int nb, int lq, int lk, int win_l, i
 }
 
 // P^T and dS^T of 16 queries of one key row: the high/low parts of P as 8 + 8
-// packed words, of dS as 8 + 8.  `masked` selects the per-element
-// visibility test (rows whose whole chunk is visible skip it).
+// packed words, of dS as 8 + 8.  Pairs of queries go through packed f32x2
+// arithmetic.  `masked` selects the per-element visibility test (rows whose
+// whole chunk is visible skip it).  lsd4: the pairs' {-LSE, -LSE, D, D}.
 template <typename T, bool kCap>
-__device__ __forceinline__ void p_ds_16(const uint32_t *su, const uint32_t *du, const float2 *lsd,
+__device__ __forceinline__ void p_ds_16(const uint32_t *su, const uint32_t *du, const float4 *lsd4,
                                         int i, int qlo, int qhi, bool masked,
                                         float sl2, float cap_in, float cap_l2, uint32_t *ph,
                                         uint32_t *pl, uint32_t *dh, uint32_t *dl) {
+  const uint64_t sl2x2 = f2_pack(sl2, sl2), cap_l2x2 = f2_pack(cap_l2, cap_l2);
 #pragma unroll
-  for (int e4 = 0; e4 < 4; ++e4) {
-    // (lse, D) of columns 4 e4 .. 4 e4 + 3: two 16-byte loads
-    const float4 a4 = reinterpret_cast<const float4 *>(lsd)[2 * e4];
-    const float4 b4 = reinterpret_cast<const float4 *>(lsd)[2 * e4 + 1];
-    const float lv[4] = {a4.x, a4.z, b4.x, b4.z}, dv4[4] = {a4.y, a4.w, b4.y, b4.w};
-#pragma unroll
-    for (int e2 = 0; e2 < 2; ++e2) {
-      float pv[2], dv[2];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = 4 * e4 + 2 * e2 + u;
-        const float s = __uint_as_float(su[c]);
-        float p, dcap = 1.f;
-        if constexpr (kCap) {
-          const float t = tanh_fast(s * cap_in);
-          p = ex2(fmaf(cap_l2, t, -lv[2 * e2 + u]));
-          dcap = 1.f - t * t;
-        } else {
-          p = ex2(fmaf(s, sl2, -lv[2 * e2 + u]));
-        }
-        if (masked && (i + c < qlo || i + c > qhi)) p = 0.f;
-        pv[u] = p;
-        dv[u] = kCap ? p * (__uint_as_float(du[c]) - dv4[2 * e2 + u]) * dcap
-                     : p * (__uint_as_float(du[c]) - dv4[2 * e2 + u]);
-      }
-      split_hi_lo<T>(pv, ph[2 * e4 + e2], pl[2 * e4 + e2]);
-      split_hi_lo<T>(dv, dh[2 * e4 + e2], dl[2 * e4 + e2]);
+  for (int q = 0; q < 8; ++q) {
+    const int c = 2 * q;
+    const float4 v = lsd4[q];
+    const uint64_t nl = f2_pack(v.x, v.y), dd = f2_pack(v.z, v.w);
+    const uint64_t s2 = f2_pack(__uint_as_float(su[c]), __uint_as_float(su[c + 1]));
+    const uint64_t dp2 = f2_pack(__uint_as_float(du[c]), __uint_as_float(du[c + 1]));
+    float t0, t1;
+    uint64_t dcap = 0;
+    if constexpr (kCap) {
+      // capped score c tanh(s / c); its derivative factor is 1 - tanh^2
+      const float h0 = tanh_fast(__uint_as_float(su[c]) * cap_in);
+      const float h1 = tanh_fast(__uint_as_float(su[c + 1]) * cap_in);
+      f2_unpack(f2_fma(cap_l2x2, f2_pack(h0, h1), nl), t0, t1);
+      dcap = f2_pack(fmaf(-h0, h0, 1.f), fmaf(-h1, h1, 1.f));
+    } else {
+      f2_unpack(f2_fma(s2, sl2x2, nl), t0, t1);
     }
+    float p0 = ex2(t0), p1 = ex2(t1);
+    if (masked) {
+      if (i + c < qlo || i + c > qhi) p0 = 0.f;
+      if (i + c + 1 < qlo || i + c + 1 > qhi) p1 = 0.f;
+    }
+    const uint64_t p2 = f2_pack(p0, p1);
+    uint64_t ds2 = f2_mul(p2, f2_sub(dp2, dd));
+    if constexpr (kCap) ds2 = f2_mul(ds2, dcap);
+    split_hi_lo<T>(p2, ph[q], pl[q]);
+    split_hi_lo<T>(ds2, dh[q], dl[q]);
   }
 }
 
@@ -178,7 +188,7 @@ __device__ __forceinline__ void p_ds_16(const uint32_t *su, const uint32_t *du, 
 // arrays at ds_hi / ds_hi + kDS.
 template <typename T, bool kCap>
 __device__ __forceinline__ void half_p_ds(uint32_t row_t, uint32_t buf, int hq, uint8_t *ds_hi,
-                                          int j, const float2 *lsd, int i0, int qlo, int qhi,
+                                          int j, const float4 *lsd4, int i0, int qlo, int qhi,
                                           float sl2, float cap_in, float cap_l2) {
   uint32_t su[32], du[32];
   tmem_ld32(row_t + buf + 32 * hq, su);
@@ -190,7 +200,7 @@ __device__ __forceinline__ void half_p_ds(uint32_t row_t, uint32_t buf, int hq, 
   for (int hv = 0; hv < 2; ++hv) {
     const int c0 = 16 * hv;
     uint32_t dh[8], dl[8];
-    p_ds_16<T, kCap>(su + c0, du + c0, lsd + c0, i0 + c0, qlo, qhi, masked, sl2, cap_in, cap_l2,
+    p_ds_16<T, kCap>(su + c0, du + c0, lsd4 + c0 / 2, i0 + c0, qlo, qhi, masked, sl2, cap_in, cap_l2,
                      ph + 8 * hv, pl + 8 * hv, dh, dl);
     // dS^T: 16 queries = two 16-byte chunks of the row's 128 bytes
 #pragma unroll
@@ -254,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.dq_free[s], 4);
     }
     mbar_init(&sh.all_done, 1);
+    sh.wait_ns = f.wait_ns;
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -298,7 +309,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int r = lane; r < BQ; r += 32) {
             const int i = i0 + r;
             const bool in = i < lq;
-            cp_async_8(&sh.lsd[st][r], a.lsd + f.seqs.lse_index(b, h, q0, in ? i : 0), in ? 8u : 0u);
+            const int64_t li = f.seqs.lse_index(b, h, q0, in ? i : 0);
+            float *dst = &sh.lsd[st][(r >> 1) * 4 + (r & 1)];
+            cp_async_4(dst, a.nlse2 + li, in ? 4u : 0u);
+            cp_async_4(dst + 2, a.dsum + li, in ? 4u : 0u);
           }
           cp_async_mbar_arrive(&sh.qd_full[st]);
           __syncwarp();
@@ -354,7 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           return r;
         };
-        bool ok = wait_bar(sh, &sh.kv_full, 0, f.err);
+        // test hook: all_done completes only after this thread's last
+        // commit, so this wait can only run out
+        bool ok = !(f.stall && !wait_bar(sh, &sh.all_done, 0, f.err));
+        ok = ok && wait_bar(sh, &sh.kv_full, 0, f.err);
         for (int it = 0; ok && it < min(2, n_iter); ++it) {
           if (!(ok = stage_ready(it))) break;
           issue_s_or_dp(it, 0);
@@ -448,11 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint8_t *ds_hi = ds_s + bf * 2 * kDS;
       const uint32_t buf = kColBuf + 128 * bf;
-      const float2 *lsd = sh.lsd[st] + 32 * w;
+      const float4 *lsd4 = reinterpret_cast<const float4 *>(sh.lsd[st]) + 16 * w;
       if (cap)
-        half_p_ds<T, true>(row_t, buf, w, ds_hi, j, lsd, i0, qlo, qhi, sl2, cap_in, cap_l2);
+        half_p_ds<T, true>(row_t, buf, w, ds_hi, j, lsd4, i0, qlo, qhi, sl2, cap_in, cap_l2);
       else
-        half_p_ds<T, false>(row_t, buf, w, ds_hi, j, lsd, i0, qlo, qhi, sl2, cap_in, cap_l2);
+        half_p_ds<T, false>(row_t, buf, w, ds_hi, j, lsd4, i0, qlo, qhi, sl2, cap_in, cap_l2);
       tmem_wait_st();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
@@ -496,6 +513,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
     // ------------------------------------------------------------ dQ
     const int dl = 32 * (warp & 3) + lane;  // TMEM lane = head-dim column
+    // the accumulator is (hq, rows, d): a chunk's rows are D floats apart
+    const int64_t rows_all = f.seqs.cu_q ? f.seqs.total_q : (int64_t)f.batch * f.seqs.sq;
     for (int it = 0; with_dq && it < n_iter; ++it) {
       const int bf = it & 1;
       const int h = kvh * g + it / nch;
@@ -509,11 +528,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive_relaxed_warp(&sh.dq_free[bf]);  // not behind the previous chunk's adds
-      float *acc = a.dq_acc + ((int64_t)(q0 + i0) * f.hq + h) * D + dl;
+      float *acc = a.dq_acc + ((int64_t)h * rows_all + q0 + i0) * D + dl;
       const int rows = min(BQ, lq - i0);
 #pragma unroll
       for (int e = 0; e < BQ; ++e)
-        if (e < rows) red_add(acc + (int64_t)e * f.hq * D, __uint_as_float(u[e]));
+        if (e < rows) red_add(acc + e * D, __uint_as_float(u[e]));
     }
   }
   tc_fence_before();
@@ -548,27 +567,29 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int64_t rows) 
         const int64_t bb = row / f.seqs.sq, i = row % f.seqs.sq;
         li = (bb * f.hq + h) * f.seqs.sq + i;
       }
-      a.lsd[li] = make_float2(f.lse[li] * kLog2e, s);
+      a.dsum[li] = s;
+      a.nlse2[li] = -(f.lse[li] * kLog2e);
     }
   }
 }
 
-// dQ = scale * dQ_acc -> dtype.
+// dQ = scale * dQ_acc -> dtype: the accumulator is (hq, rows, d), dQ
+// (rows, hq, d) with rows dq_rs elements apart.  One thread per 4 values.
 template <typename T>
-__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdArgs a, int64_t n4) {
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdArgs a, int64_t rows, int64_t n4) {
+  const int hq = a.f.hq;
   for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n4;
        x += (int64_t)gridDim.x * blockDim.x) {
-    const float4 v = reinterpret_cast<const float4 *>(a.dq_acc)[x];
+    // x walks dQ in (row, head, d / 4) order
+    const int c4 = (int)(x % (D / 4));
+    const int64_t rh = x / (D / 4);
+    const int h = (int)(rh % hq);
+    const int64_t row = rh / hq;
+    const float4 v = reinterpret_cast<const float4 *>(a.dq_acc)[(h * rows + row) * (D / 4) + c4];
     const float s = a.f.scale;
     uint2 out{Elem<T>::from_f2(v.x * s, v.y * s), Elem<T>::from_f2(v.z * s, v.w * s)};
-    // the accumulator is contiguous (rows, hq * d); dQ rows are dq_rs apart
-    const int64_t per_row = (int64_t)a.f.hq * D / 4;
-    int64_t dst = x * 4;
-    if (a.dq_rs != per_row * 4) {
-      const int64_t row = x / per_row;
-      dst = row * a.dq_rs + (x - row * per_row) * 4;
-    }
-    *reinterpret_cast<uint2 *>(static_cast<T *>(a.dq) + dst) = out;
+    *reinterpret_cast<uint2 *>(static_cast<T *>(a.dq) + row * a.dq_rs + (int64_t)h * D + c4 * 4) =
+        out;
   }
 }
 
@@ -594,6 +615,10 @@ cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
     const int n_blocks = (f.seqs.sk + BN - 1) / BN;
     const int64_t grid = (int64_t)n_blocks * f.hkv * f.batch;
     if (grid > INT32_MAX) return cudaErrorInvalidValue;
+    debug_log("backward: bwd_tc_kernel d=128, %d keys per CTA, %d-query chunks, dQ %s, "
+              "grid=%lld CTAs x %d threads, smem=%d B", BN, BQ,
+              a.deterministic ? "by the query-stationary kernel (deterministic)" : "atomic fp32 adds",
+              (long long)grid, kThreads, kSmem);
     bwd_tc_kernel<T><<<(unsigned)grid, kThreads, kSmem, st>>>(tq, tk, tv, tdo, a, n_blocks);
     count_launches(1);
   } else if (rows_k > 0) {  // no queries: the key gradients are zero
@@ -609,7 +634,7 @@ cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
   } else if (rows_q > 0) {
     const int64_t n4 = rows_q * f.hq * D / 4;
     const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, (int64_t)sms * 16);
-    bwd_dq_convert_kernel<T><<<std::max(blocks, 1), 256, 0, st>>>(a, n4);
+    bwd_dq_convert_kernel<T><<<std::max(blocks, 1), 256, 0, st>>>(a, rows_q, n4);
     count_launches(1);
   }
   return cudaGetLastError();

@@ -118,7 +118,13 @@ struct Seqs {
     }
     q0 = cu_q[b]; lq = cu_q[b + 1] - q0;
     k0 = cu_k[b]; lk = cu_k[b + 1] - k0;
-    if (lq < 0 || lk < 0) { raise_error(err, kErrBadSeqlen); return false; }
+    // offsets must stay inside the packed tensors: a sequence ending past
+    // total_q / total_k would make the output and gradient stores run off
+    // the end of the caller's buffers
+    if (lq < 0 || lk < 0 || q0 < 0 || k0 < 0 || q0 + lq > total_q || k0 + lk > total_k) {
+      raise_error(err, kErrBadSeqlen);
+      return false;
+    }
     if (lq > sq || lk > sk) { raise_error(err, kErrVarlenTooLong); return false; }
     return true;
   }

@@ -42,6 +42,28 @@ __global__ void append_kernel(DecodeArgs a) {
   }
 }
 
+// Result of a row whose keys could not be read (bad length or page): O = 0
+// and LSE = -inf, the result of an empty key set, so that the combine step
+// gives the split no weight and the output does not depend on stale scratch
+// contents.  The device error word says what happened.  One warp.
+template <typename T, int D>
+__device__ __forceinline__ void store_empty_row(const DecodeArgs &a, int split, int bi, int r,
+                                                int h, int lane) {
+  constexpr int V = D / 32;
+  float z[V];
+#pragma unroll
+  for (int u = 0; u < V; ++u) z[u] = 0.f;
+  if (a.num_splits == 1) {
+    store_vec<T, V>(static_cast<T *>(a.o) + (((int64_t)bi * a.sq + r) * a.hq + h) * D + lane * V, z);
+    if (lane == 0) a.lse[((int64_t)bi * a.hq + h) * a.sq + r] = -INFINITY;
+  } else {
+    float *op = a.o_part + (((((int64_t)split * a.b + bi) * a.sq + r) * a.hq + h) * D) + lane * V;
+#pragma unroll
+    for (int u = 0; u < V; ++u) op[u] = 0.f;
+    if (lane == 0) a.lse_part[(((int64_t)split * a.b + bi) * a.hq + h) * a.sq + r] = -INFINITY;
+  }
+}
+
 // One warp per (batch entry, query head, query row, split).
 // grid (splits, hq, b); the 4 warps of a block take rows r = warp, warp+4, ...
 template <typename T, int D>
@@ -51,9 +73,9 @@ __global__ void __launch_bounds__(kWarps * 32) decode_rows_kernel(DecodeArgs a) 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int split = blockIdx.x, h = blockIdx.y, bi = blockIdx.z;
   const int L = a.cache_seqlens[bi] + a.s_new;
-  if (L < 0) return;
-  if (L > a.max_pages * a.page_size) {
-    if (threadIdx.x == 0) raise_error(a.err, kErrCacheOverflow);
+  if (L < 0 || L > a.max_pages * a.page_size) {
+    if (threadIdx.x == 0) raise_error(a.err, L < 0 ? kErrBadSeqlen : kErrCacheOverflow);
+    for (int r = warp; r < a.sq; r += kWarps) store_empty_row<T, D>(a, split, bi, r, h, lane);
     return;
   }
   const int kvh = h / (a.hq / a.hkv);
@@ -111,7 +133,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_rows_kernel(DecodeArgs a) 
       }
       m = mnew;
     }
-    if (bad) { __syncwarp(); continue; }
+    if (bad) {
+      store_empty_row<T, D>(a, split, bi, r, h, lane);
+      __syncwarp();
+      continue;
+    }
     const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll
     for (int u = 0; u < V; ++u) acc[u] *= inv;
@@ -185,6 +211,8 @@ cudaError_t decode(const DecodeArgs &a, cudaStream_t st) {
   // tensor-core kernel (d = 128, g * sq <= 32); warp-per-row kernel otherwise
   cudaError_t e = launch_decode_tc(a, st);
   if (e == cudaErrorNotSupported) {
+    debug_log("decode: decode_rows_kernel (CUDA cores, one warp per query row) d=%d, "
+              "num_splits=%d (%d keys each)", D, a.num_splits, a.split_chunk);
     decode_rows_kernel<T, D><<<dim3(a.num_splits, a.hq, a.b), kWarps * 32, 0, st>>>(a);
     count_launches(1);
   } else if (e != cudaSuccess) {

@@ -55,6 +55,8 @@ struct DecShared {
   uint64_t k_full[ST], k_empty[ST], v_full[ST], v_empty[ST];
   uint64_t s_full[2], p_full[2], o_done;
   uint64_t grp;  // bounded barrier of the 128 softmax threads (one phase per use)
+  uint64_t all_done;  // every MMA of the CTA has completed
+  uint64_t wait_ns;   // wall-clock limit of a wait
   uint32_t tmem_base;
   int abort;
   float wmax[2][4][32];
@@ -68,7 +70,29 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 __device__ __forceinline__ bool wait_bar(DecShared &sh, uint64_t *bar, uint32_t parity, int *err) {
-  return mbar_wait_bounded(smem_u32(bar), parity, &sh.abort, err);
+  return mbar_wait_bounded(smem_u32(bar), parity, &sh.abort, err, sh.wait_ns);
+}
+
+// The result of a split whose keys could not be read (a bad length, a page
+// outside the pool, or an abandoned wait): O = 0 and LSE = -inf, what an
+// empty key set gives, so the combine step gives the split no weight and no
+// stale scratch value reaches the output.  The device error word records
+// the cause.  Thread `tid` of `nthreads` writes its share of the R rows.
+template <typename T>
+__device__ __forceinline__ void store_empty_split(const DecodeArgs &a, int split, int bi, int kvh,
+                                                  int R, int tid, int nthreads) {
+  const int g = a.hq / a.hkv;
+  for (int x = tid; x < R * D; x += nthreads) {
+    const int q = x / D, dcol = x % D;
+    const int r = q / g, h = kvh * g + q % g;
+    if (a.num_splits == 1) {
+      static_cast<T *>(a.o)[(((int64_t)bi * a.sq + r) * a.hq + h) * D + dcol] = Elem<T>::from_f(0.f);
+      if (dcol == 0) a.lse[((int64_t)bi * a.hq + h) * a.sq + r] = -INFINITY;
+    } else {
+      a.o_part[((((int64_t)split * a.b + bi) * a.sq + r) * a.hq + h) * D + dcol] = 0.f;
+      if (dcol == 0) a.lse_part[(((int64_t)split * a.b + bi) * a.hq + h) * a.sq + r] = -INFINITY;
+    }
+  }
 }
 
 // The same wait taken by a whole warp with one answer, so warp-collective
@@ -132,6 +156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int L = a.cache_seqlens[bi] + a.s_new;
   if (L < 0 || L > a.max_pages * a.page_size) {
     if (threadIdx.x == 0) raise_error(a.err, L < 0 ? kErrBadSeqlen : kErrCacheOverflow);
+    store_empty_split<T>(a, split, bi, kvh, R, threadIdx.x, kThreads);
     return;
   }
   // keys any query row may see, clipped to this split
@@ -159,6 +184,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&sh.o_done, 1);
     mbar_init(&sh.grp, 128);
+    mbar_init(&sh.all_done, 1);
+    sh.wait_ns = a.wait_ns;
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -242,7 +269,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&sh.k_empty[st]);
         return true;
       };
-      bool ok = wait_bar(sh, &sh.q_full, 0, a.err) && issue_s(0);
+      // test hook: all_done completes only after this thread's last commit,
+      // so this wait can only run out
+      bool ok = !(a.stall && !wait_bar(sh, &sh.all_done, 0, a.err));
+      ok = ok && wait_bar(sh, &sh.q_full, 0, a.err) && issue_s(0);
       for (int j = 0; ok && j < n; ++j) {
         if (j + 1 < n && !issue_s(j + 1)) break;
         if (!wait_bar(sh, &sh.p_full[j & 1], (j >> 1) & 1, a.err)) break;
@@ -259,6 +289,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&sh.o_done);
         mma_commit(&sh.v_empty[st]);
+      }
+      // after an abort, no MMA may still run when the TMEM is released
+      mma_commit(&sh.all_done);
+      if (*(volatile int *)&sh.abort) {
+        int *noerr = nullptr;
+        mbar_wait(&sh.all_done, 0, noerr);
       }
     }
   } else {
@@ -420,6 +456,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (jl == 0) a.lse_part[(((int64_t)split * a.b + bi) * a.hq + h) * a.sq + r] = lse;
         }
       }
+    } else {
+      store_empty_split<T>(a, split, bi, kvh, R, jl, 128);
     }
   }
   tc_fence_before();
@@ -452,6 +490,9 @@ cudaError_t decode_tc(const DecodeArgs &a, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   const int64_t grid = (int64_t)a.num_splits * a.hkv * a.b;
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
+  debug_log("decode: decode_tc_kernel d=128, %d query rows (g*sq) padded to %d, %d-key tiles, "
+            "num_splits=%d (%d keys each), grid=%lld CTAs x %d threads", (a.hq / a.hkv) * a.sq,
+            RP, BK, a.num_splits, a.split_chunk, (long long)grid, kThreads);
   decode_tc_kernel<T, RP><<<(unsigned)grid, kThreads, C::kSmem, st>>>(tq, tk, tv, a);
   count_launches(1);
   return cudaGetLastError();

@@ -27,6 +27,8 @@
 // tiles are shared through L2.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "kernels.h"
 #include "sm103.cuh"
 
@@ -100,6 +102,8 @@ struct Shared {
   uint64_t q_full;
   uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
   uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t all_done;  // every MMA of the CTA has completed
+  uint64_t wait_ns;   // wall-clock limit of a wait
   uint32_t tmem_base;
   int abort;
 };
@@ -112,7 +116,7 @@ __device__ __forceinline__ float ex2(float x) {
 
 // Bounded wait that also gives up when another role has aborted.
 __device__ __forceinline__ bool wait_bar(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
-  return mbar_wait_bounded(smem_u32(bar), parity, &sh.abort, err);
+  return mbar_wait_bounded(smem_u32(bar), parity, &sh.abort, err, sh.wait_ns);
 }
 
 // The same wait taken by a whole warp with one answer, so warp-collective
@@ -159,17 +163,51 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
   if (m0 >= lq) return;
   const int kvh = pg > 1 ? hh : hh / (a.hq / a.hkv);
   const int h = pg > 1 ? kvh * pg : hh;  // (first) query head of the tile rows
-  const int m_last = min(m0 + tile_pos * NT, lq) - 1;
 
-  // key tiles any row of this query block may see
-  int lo_first, hi_first, lo_last, hi_last;
-  key_range(m0, lq, lk, a.win_l, a.win_r, lo_first, hi_first);
-  key_range(m_last, lq, lk, a.win_l, a.win_r, lo_last, hi_last);
+  // Key tiles each query tile may see: [t_lo, t_hi] from its first and last
+  // valid rows (the visible range's ends never decrease down the rows), and
+  // their union [n_lo, n_lo + nt), which the producer streams.  Tile t runs
+  // the steps [ta, tb) of the union, so a tile never computes a key tile
+  // that none of its rows sees (e.g. the diagonal tile of the next query
+  // tile under a causal mask, or the tiles left of a sliding window).
+  auto tile_keys = [&](int t, int &t_lo, int &t_hi) {
+    const int first = m0 + t * tile_pos, last = min(first + tile_pos, lq) - 1;
+    t_lo = 0;
+    t_hi = -1;
+    if (first < lq) {
+      int lo_f, hi_f, lo_l, hi_l;
+      key_range(first, lq, lk, a.win_l, a.win_r, lo_f, hi_f);
+      key_range(last, lq, lk, a.win_l, a.win_r, lo_l, hi_l);
+      if (hi_l >= lo_f && hi_l >= 0) {
+        t_lo = lo_f / BN;
+        t_hi = hi_l / BN;
+      }
+    }
+  };
   int n_lo = 0, nt = 0;
-  if (hi_last >= lo_first && hi_last >= 0) {
-    n_lo = lo_first / BN;
-    nt = hi_last / BN - n_lo + 1;
+  {
+    int u_lo = INT_MAX, u_hi = -1;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      int t_lo, t_hi;
+      tile_keys(t, t_lo, t_hi);
+      if (t_hi >= t_lo) {
+        u_lo = min(u_lo, t_lo);
+        u_hi = max(u_hi, t_hi);
+      }
+    }
+    if (u_hi >= 0) {
+      n_lo = u_lo;
+      nt = u_hi - u_lo + 1;
+    }
   }
+  // steps [ta, tb) of the union that tile t takes part in
+  auto tile_steps = [&](int t, int &ta, int &tb) {
+    int t_lo, t_hi;
+    tile_keys(t, t_lo, t_hi);
+    ta = t_hi >= t_lo ? t_lo - n_lo : 0;
+    tb = t_hi >= t_lo ? t_hi - n_lo + 1 : 0;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(&sh.q_full, 1);
@@ -184,6 +222,8 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
       mbar_init(&sh.p_full[s], kBM);
       mbar_init(&sh.o_done[s], 1);
     }
+    mbar_init(&sh.all_done, 1);
+    sh.wait_ns = a.wait_ns;
     sh.abort = 0;
     fence_mbar_init();
   }
@@ -197,11 +237,12 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
   const uint32_t tmem = sh.tmem_base;
   // NT = 2 is launched at 168 registers a thread (12 warps).  The producer/MMA
   // warpgroup gives registers to the softmax warpgroups, which hold a whole
-  // 128-score row: 128 * 64 + 256 * 216 <= 384 * 168.  Each setmaxnreg sits at
-  // the head of its warpgroup's branch, so every role's code is compiled for
-  // its own register budget.
+  // 128-score row: 128 * 88 + 256 * 208 = 384 * 168 (88 is the least at
+  // which the MMA issuer's loop needs no spill).  Each setmaxnreg sits at the
+  // head of its warpgroup's branch, so every role's code is compiled for its
+  // own register budget.
   if (warp < C::kSoftmaxWarp0) {
-  if constexpr (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 64;" ::: "memory");
+  if constexpr (NT == 2) asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // (no key tile visible: nothing is loaded, so no copy outlives the CTA)
@@ -266,13 +307,14 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
             mma_ss(dcol, ad, bd, id_s, kk > 0);
         }
       };
-      // O_t += P V_j with P read from TMEM column `pcol`
-      auto mma_pv = [&](int t, int j, uint32_t pcol) {
+      // O_t (+)= P V_j with P read from TMEM column `pcol`; `first`: the
+      // tile's first key tile, which starts the accumulation
+      auto mma_pv = [&](int t, int j, uint32_t pcol, bool first) {
         const uint32_t vo = (j % ST) * C::kKVBytes;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
           const uint64_t bd = desc_add(v_d, vo + kk * 16 * 128);
-          mma_ts(tmem + t * D, pcol + kk * 8, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + t * D, pcol + kk * 8, bd, id_o, (!first || kk > 0) ? 1u : 0u);
         }
       };
       auto k_ready = [&](int j) {
@@ -285,31 +327,60 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
         tc_fence_after();
         return r;
       };
-      if (NT == 2) {
-        // S_0(0) S_1(0) | PV_0(j) S_0(j+1) PV_1(j) S_1(j+1) | ...
+      int ta[NT], tb[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) tile_steps(t, ta[t], tb[t]);
+      // test hook: all_done completes only after this thread's last commit,
+      // so this wait can only run out (then every role takes the abort path)
+      const bool stalled = a.stall && !wait_bar(sh, &sh.all_done, 0, a.err);
+      if (stalled) {
+      } else if (NT == 2) {
+        // S_0(0) S_1(0) | PV_0(j) S_0(j+1) PV_1(j) S_1(j+1) | ..., where a
+        // tile takes part in step j only inside its own range [ta, tb).
+        // Every K and V tile of the union is waited for once before its
+        // stage is released, whether or not a tile used it.
         bool ok = nt == 0 || (wait_bar(sh, &sh.q_full, 0, a.err) && k_ready(0));
         if (ok && nt > 0) {
           for (int t = 0; t < NT; ++t) {
-            mma_s(t, 0, tmem + C::kSCol0 + t * BN);
-            mma_commit(&sh.s_full[t]);
+            if (ta[t] == 0 && tb[t] > 0) {
+              mma_s(t, 0, tmem + C::kSCol0 + t * BN);
+              mma_commit(&sh.s_full[t]);
+            }
           }
           mma_commit(&sh.k_empty[0]);
         }
         for (int j = 0; ok && j < nt; ++j) {
+          const bool k_next = j + 1 < nt;
+          // the last tile that reads V_j / K_{j+1} releases its stage
+          const int last_pv = (j >= ta[1] && j < tb[1]) ? 1 : 0;
+          const int last_s = (j + 1 >= ta[1] && j + 1 < tb[1]) ? 1 : 0;
+          bool v_in = false, k_in = false;
           for (int t = 0; t < NT && ok; ++t) {
             const uint32_t scol = tmem + C::kSCol0 + t * BN;
-            if (!wait_bar(sh, &sh.p_full[t], j & 1, a.err)) { ok = false; break; }
-            tc_fence_after();
-            if (t == 0 && !v_ready(j)) { ok = false; break; }
-            mma_pv(t, j, scol);
-            mma_commit(&sh.o_done[t]);
-            if (t == NT - 1) mma_commit(&sh.v_empty[j % ST]);
-            if (j + 1 < nt) {
-              if (t == 0 && !k_ready(j + 1)) { ok = false; break; }
+            if (j >= ta[t] && j < tb[t]) {
+              if (!wait_bar(sh, &sh.p_full[t], (j - ta[t]) & 1, a.err)) { ok = false; break; }
+              tc_fence_after();
+              if (!v_in && !(v_in = v_ready(j))) { ok = false; break; }
+              mma_pv(t, j, scol, j == ta[t]);
+              mma_commit(&sh.o_done[t]);
+              if (t == last_pv) mma_commit(&sh.v_empty[j % ST]);
+            }
+            if (k_next && j + 1 >= ta[t] && j + 1 < tb[t]) {
+              if (!k_in && !(k_in = k_ready(j + 1))) { ok = false; break; }
               mma_s(t, j + 1, scol);
               mma_commit(&sh.s_full[t]);
-              if (t == NT - 1) mma_commit(&sh.k_empty[(j + 1) % ST]);
+              if (t == last_s) mma_commit(&sh.k_empty[(j + 1) % ST]);
             }
+          }
+          // a tile of the union that no query tile read still has to land
+          // before its stage is handed back
+          if (ok && !v_in) {
+            if (!v_ready(j)) break;
+            mma_commit(&sh.v_empty[j % ST]);
+          }
+          if (ok && k_next && !k_in) {
+            if (!k_ready(j + 1)) break;
+            mma_commit(&sh.k_empty[(j + 1) % ST]);
           }
         }
       } else {
@@ -329,15 +400,23 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
           if (!wait_bar(sh, &sh.p_full[j & 1], (j >> 1) & 1, a.err)) break;
           tc_fence_after();
           if (!v_ready(j)) break;
-          mma_pv(0, j, tmem + C::kSCol0 + (j & 1) * BN);
+          mma_pv(0, j, tmem + C::kSCol0 + (j & 1) * BN, j == 0);
           mma_commit(&sh.o_done[0]);
           mma_commit(&sh.v_empty[j % ST]);
         }
       }
+      // completes when every MMA above has; after an abort, wait for it so
+      // that no MMA still reads shared memory or writes TMEM when the CTA
+      // releases its TMEM and exits
+      mma_commit(&sh.all_done);
+      if (*(volatile int *)&sh.abort) {
+        int *noerr = nullptr;
+        mbar_wait(&sh.all_done, 0, noerr);
+      }
     }
   }
   } else {
-    if constexpr (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 216;" ::: "memory");
+    if constexpr (NT == 2) asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
     // ------------------------------------------------------------ softmax
     const int t = (warp - C::kSoftmaxWarp0) >> 2;  // query tile of this warpgroup
     const int r = 32 * (warp & 3) + lane;  // TMEM lane = row in the tile
@@ -356,8 +435,12 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
     const float cap_in = cap ? a.scale / a.softcap : 0.f, cap_out = a.softcap * kLog2e;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < nt; ++j) {
-      const int key0 = (n_lo + j) * BN;
+    // this tile's own key tiles: n_lo + ta + j for j in [0, ntt)
+    int ta, tb;
+    tile_steps(t, ta, tb);
+    const int ntt = tb - ta;
+    for (int j = 0; j < ntt; ++j) {
+      const int key0 = (n_lo + ta + j) * BN;
       const int sb = NT == 2 ? t : (j & 1);                 // S/P buffer and its barriers
       const uint32_t s_par = NT == 2 ? (j & 1) : ((j >> 1) & 1);
       if (!wait_warp(sh, &sh.s_full[sb], s_par, a.err)) { ok = false; break; }
@@ -387,14 +470,22 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
         }
       }
       // raw-score max: scale and softcap preserve the order (scale >= 0);
-      // eight independent partial maxima keep the dependency chains short
+      // eight independent partial maxima of three-input maxes keep the
+      // dependency chains short
       float mp[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) mp[u] = x[u];
 #pragma unroll
-      for (int e = 8; e < BN; ++e) mp[e & 7] = fmaxf(mp[e & 7], x[e]);
-      const float mt = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      for (int e = 8; e + 16 <= BN; e += 16) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mp[u] = fmax3(mp[u], x[e + u], x[e + 8 + u]);
+      }
+      if constexpr ((BN - 8) % 16 != 0) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) mp[u] = fmaxf(mp[u], x[BN - 8 + u]);
+      }
+      const float mt = fmaxf(fmax3(mp[0], mp[1], mp[2]),
+                             fmax3(fmax3(mp[3], mp[4], mp[5]), mp[6], mp[7]));
       const float f = cap ? 1.f : sl2;  // x * f is the score in log2 units
       const float m_new = fmaxf(m_ref, mt * f);
       const bool rescale = m_new > m_ref + kRescaleThreshold;
@@ -405,23 +496,31 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
         m_ref = m_new;
       }
       const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
-      float rs[8];
+      // t = x f - m and the row sums two at a time (packed f32x2)
+      const uint64_t f2 = f2_pack(f, f), nm2 = f2_pack(neg_m, neg_m);
+      uint64_t rs[4];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) rs[u] = 0.f;
+      for (int u = 0; u < 4; ++u) rs[u] = 0ull;
 #pragma unroll
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = ex2(fmaf(x[c * 32 + 2 * e], f, neg_m));
-          const float p1 = ex2(fmaf(x[c * 32 + 2 * e + 1], f, neg_m));
-          rs[(2 * e) & 7] += p0;
-          rs[(2 * e + 1) & 7] += p1;
+          const int el = c * 32 + 2 * e;
+          float t0, t1;
+          f2_unpack(f2_fma(f2_pack(x[el], x[el + 1]), f2, nm2), t0, t1);
+          const float p0 = ex2(t0), p1 = ex2(t1);
+          rs[e & 3] = f2_add(rs[e & 3], f2_pack(p0, p1));
           pk[e] = pack2<T>(p0, p1);
         }
         tmem_st16(scol + c * 16, pk);
       }
-      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+      {
+        float r[8];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) f2_unpack(rs[u], r[2 * u], r[2 * u + 1]);
+        l += ((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7]));
+      }
       tmem_wait_st();
       if (j > 0) {
         // O holds P_{j-1} V_{j-1} once this completes; only then may it be rescaled
@@ -444,7 +543,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
       mbar_arrive(&sh.p_full[sb]);
     }
     // epilogue: O / l -> dtype, LSE = ln(sum exp(s))
-    if (ok && nt > 0) ok = wait_warp(sh, &sh.o_done[t], (nt - 1) & 1, a.err);
+    if (ok && ntt > 0) ok = wait_warp(sh, &sh.o_done[t], (ntt - 1) & 1, a.err);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     if (ok) {
@@ -455,7 +554,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t u[32];
-        if (nt > 0) {
+        if (ntt > 0) {
           tmem_ld32(o_t + c * 32, u);
           tmem_wait_ld();
         } else {
@@ -504,6 +603,10 @@ cudaError_t fwd_tc(const FwdArgs &a, cudaStream_t st) {
   const int64_t grid = (int64_t)m_blocks * (pg > 1 ? a.hkv : a.hq) * a.batch;
   if (grid == 0) return cudaSuccess;
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
+  debug_log("forward: fwd_tc_kernel d=%d, %d query tile(s) of 128 rows per CTA, %d-key tiles, "
+            "%d-stage K/V ring, QK^T %s, pack_gqa=%d, grid=%lld CTAs x %d threads, smem=%d B",
+            D, NT, BN, C::kStages, QB == 1 ? "e4m3 (kind::f8f6f4)" : "16-bit (kind::f16)", pg,
+            (long long)grid, C::kThreads, C::kSmem);
   fwd_tc_kernel<T, D, BN, NT, QB><<<(unsigned)grid, C::kThreads, C::kSmem, st>>>(tq, tk, tv, a,
                                                                           m_blocks);
   count_launches(1);

@@ -31,6 +31,11 @@ struct FwdArgs {
   // (the V descale).  0 / 0.f: the plain 16-bit forward.
   int qk_fp8;
   float out_scale;
+  // wall-clock limit of a device-side wait (ns); set by the C ABI
+  uint64_t wait_ns;
+  // test hook (attn_set_test_stall): the MMA issuer first waits on a barrier
+  // that nothing completes, so the wait limit runs out
+  int stall;
 };
 
 // Storage code of E4M3 tensors for make_map_3d (beside ATTN_F16 / ATTN_BF16).
@@ -40,9 +45,9 @@ struct BwdArgs {
   FwdArgs f;             // f.o / f.lse are the forward's outputs (read only)
   const void *dout;
   void *dq, *dk, *dv;
-  float *dsum;           // workspace: D_i = rowsum(dO * O), LSE layout (CUDA-core path)
-  float2 *lsd;           // workspace: (LSE_i * log2(e), D_i), LSE layout (tensor-core path)
-  float *dq_acc;         // workspace: fp32 dQ accumulator (atomic mode)
+  float *dsum;           // workspace: D_i = rowsum(dO * O), LSE layout
+  float *nlse2;          // workspace: -LSE_i * log2(e), LSE layout (tensor-core path)
+  float *dq_acc;         // workspace: fp32 dQ accumulator (hq, rows, d) (atomic mode)
   int deterministic;
   int64_t dq_rs, dk_rs, dv_rs;  // token strides of the gradients (as q_rs ...)
 };
@@ -62,6 +67,8 @@ struct DecodeArgs {
   float *o_part;                // (splits, b, sq, hq, d) fp32 when num_splits > 1
   float *lse_part;              // (splits, b, hq, sq)
   int *err;
+  uint64_t wait_ns;             // wall-clock limit of a device-side wait (ns)
+  int stall;                    // test hook, as FwdArgs::stall
 };
 
 // cuTensorMapEncodeTiled from the driver (looked up once), or nullptr.
@@ -71,13 +78,19 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 // row_stride: elements between consecutive rows (0: heads * d, contiguous).
 bool make_map_3d(CUtensorMap *m, const void *base, int dtype, int64_t rows, int heads, int d,
                  int box_rows, int64_t row_stride = 0, int box_heads = 1);
-// dQ of the backward, query-stationary (d = 128): written once, no atomics.
-cudaError_t launch_bwd_dq_tc(const BwdArgs &a, cudaStream_t st);
 // Tensor-core decode; cudaErrorNotSupported for shapes it does not handle.
 cudaError_t launch_decode_tc(const DecodeArgs &a, cudaStream_t st);
 
 // Adds n to the library's launch counter (attn_launch_count).
 void count_launches(int n);
+
+// LIBATTN_DEBUG set to a non-zero number in the environment (read once, at
+// the first use) makes every launcher print the kernel, tile shape, pack
+// factor or split count and grid it chose, one line on stderr per launch
+// decision (the counterpart of FLASH_ATTN_DEBUG in Inference Cookbook FAQ
+// Q13).  debug_log is printf-like and does nothing when it is off.
+bool debug_enabled();
+void debug_log(const char *fmt, ...);
 
 // Raises `Kernel`'s dynamic shared memory limit to `bytes`, once per device:
 // later calls (including ones made during CUDA graph capture) only read a
@@ -97,6 +110,8 @@ cudaError_t set_smem_once(int bytes) {
 
 cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t st);
 cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t st);
+// dQ of the backward, query-stationary (d = 128): written once, no atomics.
+cudaError_t launch_bwd_dq_tc(const BwdArgs &a, cudaStream_t st);
 // Backward on the tensor cores (d = 128): preprocess, key-stationary dK/dV
 // kernel (with atomic dQ unless deterministic), dQ finish.
 cudaError_t launch_bwd_tc(const BwdArgs &a, int sms, cudaStream_t st);

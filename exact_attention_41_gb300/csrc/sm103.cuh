@@ -15,7 +15,9 @@
 namespace attn {
 namespace sm103 {
 
-// Upper bound of any single wait, in nanoseconds.
+// Default upper bound of a single wait, in nanoseconds.  Calls pass their
+// own limit (attn_set_wait_limit_ns); the waits that drain a CTA's own copies
+// and MMAs before it exits always use this one.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -92,11 +94,11 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 
 // Waits until the phase with the given parity has completed.  Gives up
 // (returns false) when the shared flag `*abort` is set by another role, or
-// after kWaitLimitNs of wall clock, raising kErrTimeout and setting *abort.
+// after limit_ns of wall clock, raising kErrTimeout and setting *abort.
 // The wall clock is read only once every 256 failed tests: a %globaltimer
 // read costs far more than an mbarrier test, and most waits end before it.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t a, uint32_t parity, int *abort,
-                                                  int *err) {
+                                                  int *err, uint64_t limit_ns = kWaitLimitNs) {
   uint64_t t0 = 0;
   for (uint32_t spin = 0;; ++spin) {
     if (mbar_test(a, parity)) return true;
@@ -105,7 +107,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t a, uint32_t parity, i
       const uint64_t now = globaltimer();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > kWaitLimitNs) {
+      } else if (now - t0 > limit_ns) {
         raise_error(err, kErrTimeout);
         if (abort) *(volatile int *)abort = 1;
         return false;
@@ -114,11 +116,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t a, uint32_t parity, i
   }
 }
 
+// Wait with the default limit and no abort flag: for draining a CTA's own
+// TMA copies and MMAs, which complete by themselves.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *err) {
-  return mbar_wait_bounded(smem_u32(bar), parity, nullptr, err);
+  return mbar_wait_bounded(smem_u32(bar), parity, nullptr, err, kWaitLimitNs);
 }
 
 // ------------------------------------------------------------------ cp.async
+
+// 4-byte global -> shared copy; src_bytes = 0 writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async_4(void *dst, const void *src, uint32_t src_bytes) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
 
 // 8-byte global -> shared copy; src_bytes = 0 writes zeros and reads nothing.
 __device__ __forceinline__ void cp_async_8(void *dst, const void *src, uint32_t src_bytes) {
@@ -312,6 +323,47 @@ __device__ __forceinline__ float tanh_fast(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * 2.8853900817779268f));  // 2 log2(e)
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(e + 1.f));
   return fmaf(-2.f, r, 1.f);
+}
+
+// ------------------------------------------------------------------ f32x2
+// Two fp32 values in one 64-bit register: sm_100-family FMA-pipe
+// instructions (add/mul/fma .f32x2, round to nearest) work on both in one
+// issue slot, each lane rounded exactly as the scalar instruction would.
+
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// max(a, b, c) in one instruction (a NaN operand is ignored, as in fmaxf).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 // Named barrier among `nthreads` threads (multiple of 32).

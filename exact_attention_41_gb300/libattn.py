@@ -50,6 +50,8 @@ _SIGS = {
     "attn_kvcache_advance": ([_vp, _i, _i, _vp], _i),
     "attn_get_device_error": ([_vp, ctypes.POINTER(_i)], _i),
     "attn_launch_count": ([], ctypes.c_ulonglong),
+    "attn_set_wait_limit_ns": ([ctypes.c_ulonglong], ctypes.c_ulonglong),
+    "attn_set_test_stall": ([_i], _i),
 }
 
 _lib = None
@@ -323,6 +325,18 @@ def num_splits(b, sq, hq, hkv, d, max_seqlen_k, requested=0) -> int:
 def launch_count() -> int:
     """Kernels the library has enqueued since it was loaded."""
     return int(lib().attn_launch_count())
+
+
+def set_wait_limit_ns(ns: int) -> int:
+    """Wall-clock limit of each device-side wait for the calls that follow
+    (0 = the default 2 s); returns the previous limit.  For error-path tests."""
+    return int(lib().attn_set_wait_limit_ns(int(ns)))
+
+
+def set_test_stall(on: bool) -> bool:
+    """Test hook: while on, the tensor-core kernels' first wait can only run
+    out (see attn_set_test_stall); returns the previous setting."""
+    return bool(lib().attn_set_test_stall(int(bool(on))))
 
 
 def device_error() -> tuple[int, int]:

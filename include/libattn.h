@@ -304,6 +304,31 @@ attn_status attn_get_device_error(attn_stream_t stream, int *detail);
  */
 unsigned long long attn_launch_count(void);
 
+/*
+ * Sets the wall-clock limit (nanoseconds) of every device-side wait of the
+ * calls that follow (all devices, all threads); 0 restores the default of
+ * 2 s.  Returns the previous limit.  Host only; the limit is read when a call
+ * is made, so it does not change work already enqueued.  A wait that reaches
+ * the limit gives up, its kernel skips the rest of its work, and the call's
+ * outputs are unspecified; attn_get_device_error() then reports
+ * ATTN_ERR_TIMEOUT.  Meant for tests of that error path: a very small limit
+ * makes ordinary waits expire.  (The library's own guard against a kernel
+ * that never finishes, not a counterpart of anything on the pages.)
+ */
+unsigned long long attn_set_wait_limit_ns(unsigned long long ns);
+
+/*
+ * Test hook for that error path (not for production use): while `on` is
+ * non-zero, the tensor-core kernels of the calls that follow make their MMA
+ * issuer first wait on a barrier that nothing completes, so that wait runs
+ * out after the wait limit, the kernel abandons its work (draining its own
+ * copies and MMAs first) and the call's outputs are unspecified;
+ * attn_get_device_error() then reports ATTN_ERR_TIMEOUT.  Kernels on the
+ * CUDA cores do not wait and are unaffected.  Returns the previous setting.
+ * Host only; read when a call is made.
+ */
+int attn_set_test_stall(int on);
+
 #ifdef __cplusplus
 }
 #endif

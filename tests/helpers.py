@@ -7,7 +7,8 @@ Tolerances (elementwise, against the float64 oracle):
   LSE (fp32): |gpu - ref| <= 1e-3, and -inf exactly where the oracle has -inf.
 The FlashAttention FAQ's own reference tolerances (Inference Cookbook Q10:
 fp16 1e-3/1e-3, bf16 5e-3/5e-3) are tighter; `report` records how a result
-fares against those too.
+fares against both, without asserting, and the test session prints the
+table at its end (tests/conftest.py).
 """
 import numpy as np
 
@@ -71,3 +72,28 @@ def assert_lse(got, want, what="lse"):
 
 def max_err(got, want):
     return float(np.max(np.abs(np.asarray(got, np.float64) - np.asarray(want, np.float64))))
+
+
+# (name, reference, dtype, max |err|, worst err/bound and fraction out of
+# bound for the contract, the same for the FAQ's tolerances)
+ACCURACY = []
+
+
+def error_stats(got, want, dtype):
+    """Max |err| and, for the contract and the FAQ Q10 tolerances, the worst
+    err / bound ratio and the fraction of elements above the bound."""
+    got = np.asarray(got, dtype=np.float64)
+    want = np.asarray(want, dtype=np.float64)
+    err = np.abs(got - want)
+    out = {"max_abs_err": float(err.max()) if err.size else 0.0}
+    for name, (atol, rtol) in (("contract", TOL[dtype]), ("pages_q10", PAGE_TOL[dtype])):
+        bound = atol + rtol * np.abs(want)
+        out[name] = {"worst_ratio": float((err / bound).max()) if err.size else 0.0,
+                     "frac_out": float((err > bound).mean()) if err.size else 0.0}
+    return out
+
+
+def report(name, got, want, dtype, reference="oracle (stored-O reading of D)"):
+    """Records how `got` compares with `want` against both tolerance sets;
+    asserts nothing."""
+    ACCURACY.append((name, reference, dtype, error_stats(got, want, dtype)))

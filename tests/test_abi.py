@@ -137,17 +137,21 @@ def test_fp8_host_checks(lib):
 
 def test_split_heuristic_on_host(lib):
     """Inference Cookbook FAQ Q14's split rules as implemented (host logic;
-    without a GPU the library assumes the GB300's 152 SMs): enough (batch, KV
-    head) units and short caches -> one split; long caches -> 8192-key pieces;
-    few units -> at least SMs / units splits, never more than 128-key tiles."""
+    the SM count is the present GPU's, 152 -- the GB300's -- without one):
+    enough (batch, KV head) units and short caches -> one split; long caches
+    -> 8192-key pieces; few units -> at least SMs / units splits, never more
+    than 128-key tiles; an explicit request wins."""
+    sms = 152
     if libattn_has_device():
-        pytest.skip("the SM count of the present GPU decides")
+        import torch
+
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
     ns = lambda b, hkv, cap, n=0: lib.attn_kvcache_num_splits(b, 1, 32, hkv, 128, cap, n)
-    assert ns(64, 8, 4096) == 1
-    assert ns(64, 8, 33024) == 5
-    assert ns(1, 8, 4096) == 19          # ceil(152 / 8)
-    assert ns(1, 8, 1000) == 8           # capped by the 8 key tiles
-    assert ns(64, 8, 33024, 3) == 3      # explicit request wins
+    assert ns(64, 8, 4096) == (1 if 64 * 8 >= sms else -(-sms // 512))
+    assert ns(64, 8, 33024) == max(5, -(-sms // 512))
+    assert ns(1, 8, 4096) == min(-(-sms // 8), 32)   # ceil(SMs / units), <= 32 tiles
+    assert ns(1, 8, 1000) == 8                       # capped by the 8 key tiles
+    assert ns(64, 8, 33024, 3) == 3
 
 
 def libattn_has_device():

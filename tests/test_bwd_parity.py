@@ -9,7 +9,7 @@ import pytest
 
 from exact_attention_41_gb300 import synthetic as syn
 from oracle import attention as ref
-from tests.helpers import assert_close, dev, f64, host
+from tests.helpers import assert_close, dev, f64, host, report
 
 pytestmark = pytest.mark.gpu
 
@@ -70,6 +70,16 @@ def test_training_shape_sampled_groups(deterministic):
         bi, kv = int(rng.integers(b)), int(rng.integers(hkv))
         rq, rk, rv = ref.backward_group(q, k, v, do, bi, kv, 1 / math.sqrt(d), causal=True,
                                         stored_o=syn.BF16)
-        assert_close(host(dq[bi, :, kv * g:(kv + 1) * g]), rq, syn.BF16, "dq")
-        assert_close(host(dk[bi, :, kv]), rk, syn.BF16, "dk")
-        assert_close(host(dv[bi, :, kv]), rv, syn.BF16, "dv")
+        got = (host(dq[bi, :, kv * g:(kv + 1) * g]), host(dk[bi, :, kv]), host(dv[bi, :, kv]))
+        mode = "det" if deterministic else "atomic"
+        for n, x, r in zip(("dq", "dk", "dv"), got, (rq, rk, rv)):
+            report(f"training bwd {n} {mode} (b={bi}, kv={kv})", x, r, syn.BF16)
+        if not deterministic:
+            # the exact gradient (D from the exact O), reported only
+            eq, ek, ev = ref.backward_group(q, k, v, do, bi, kv, 1 / math.sqrt(d), causal=True)
+            for n, x, r in zip(("dq", "dk", "dv"), got, (eq, ek, ev)):
+                report(f"training bwd {n} {mode} (b={bi}, kv={kv})", x, r, syn.BF16,
+                       "oracle, exact gradient")
+        assert_close(got[0], rq, syn.BF16, "dq")
+        assert_close(got[1], rk, syn.BF16, "dk")
+        assert_close(got[2], rv, syn.BF16, "dv")

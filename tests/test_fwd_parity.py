@@ -6,7 +6,7 @@ import pytest
 
 from exact_attention_41_gb300 import synthetic as syn
 from oracle import attention as ref
-from tests.helpers import assert_close, assert_lse, dev, f64, host
+from tests.helpers import assert_close, assert_lse, dev, f64, host, report
 
 pytestmark = pytest.mark.gpu
 
@@ -90,5 +90,6 @@ def test_training_shape_sampled_rows():
     bi, hi, ri = (torch.as_tensor(x, device="cuda") for x in zip(*samples))
     q, k, v = (f64(case[x], syn.BF16) for x in ("q", "k", "v"))
     ro, rl = ref.forward_rows(q, k, v, samples, 1 / math.sqrt(d), causal=True)
+    report("training fwd O (260 sampled rows)", host(o[bi, ri, hi]), ro, syn.BF16, "oracle")
     assert_close(host(o[bi, ri, hi]), ro, syn.BF16, "out")
     assert_lse(host(lse[bi, hi, ri]), rl)

@@ -6,7 +6,7 @@ import pytest
 
 from exact_attention_41_gb300 import synthetic as syn
 from oracle import attention as ref
-from tests.helpers import assert_close, assert_lse, dev, dev_i32, f64, host
+from tests.helpers import assert_close, assert_lse, dev, dev_i32, f64, host, report
 
 pytestmark = pytest.mark.gpu
 
@@ -63,6 +63,16 @@ def test_workload_sampled_sequences(deterministic):
                                      stored_o=syn.BF16)
     cu = case["cu_seqlens_q"]
     rows = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in seqs])
+    mode = "det" if deterministic else "atomic"
+    got = {"dq": host(dq)[rows], "dk": host(dk)[rows], "dv": host(dv)[rows]}
+    report(f"varlen fwd O ({len(seqs)} sequences)", host(o)[rows], ro[rows], syn.BF16, "oracle")
+    for n, r in zip(("dq", "dk", "dv"), (rq, rk, rv)):
+        report(f"varlen bwd {n} {mode} ({len(seqs)} sequences)", got[n], r[rows], syn.BF16)
+    if not deterministic:
+        eq, ek, ev = ref.varlen_backward(*args, f64(case["dout"], syn.BF16), *a, seqs=seqs)
+        for n, r in zip(("dq", "dk", "dv"), (eq, ek, ev)):
+            report(f"varlen bwd {n} {mode} ({len(seqs)} sequences)", got[n], r[rows], syn.BF16,
+                   "oracle, exact gradient")
     assert_close(host(o)[rows], ro[rows], syn.BF16, "out")
     assert_lse(host(lse)[:, rows], rl[:, rows])
     assert_close(host(dq)[rows], rq[rows], syn.BF16, "dq")
