@@ -13,7 +13,7 @@ decode workload (HBM GB/s), an end-to-end pass through the public API from
 pinned host buffers, and the float64 CPU oracle on a bounded sample.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
-       python bench.py --profile-case fwd|bwd|decode   (one small case for ncu)
+       python bench.py --profile-case fwd|bwd|decode|varlen   (one small case for ncu)
 Under torchrun each rank runs its own replica (weak scaling) and rank 0
 prints one JSON line.
 """
@@ -638,12 +638,19 @@ def run_ours(args, rank, world, local_rank):
 
 def run_profile_case(args):
     """One small, fixed case of one kernel family, for profiler captures
-    (no timing, no JSON line): `--profile-case fwd|bwd` runs the causal
-    bf16 b=1 s=8192 hq=32 hkv=8 d=128 problem (`--deterministic` for that
-    backward mode), `decode` the paged decode of b=8, sq=s_new=4, hq=32 (the
-    workload's heads), caches U[1,32768] -- each larger than L2 in its K/V or
-    Q/dO streams and about 1 GB on the device at most.  `--calls` calls (a
-    warm-up and the one to capture), then the device error word is checked."""
+    (no timing, no JSON line); each is larger than L2 in its K/V or Q/dO
+    streams and about 1 GB on the device at most:
+
+    fwd / bwd   causal bf16 b=1 s=8192 hq=32 hkv=8 d=128 (`--deterministic`
+                for that backward mode)
+    decode      paged decode b=16, sq=s_new=4, hq=32 hkv=8, caches U[1,32768]
+                in 256-token pages (the workload's per-entry shape; 16 entries
+                make several full waves of splits)
+    varlen      the varlen workload (64 sequences U[100,4096], window (256,0),
+                softcap 50), forward then backward
+
+    `--calls` calls (a warm-up and the one to capture), then the device
+    error word is checked."""
     import torch
 
     from exact_attention_41_gb300 import build as build_mod
@@ -666,8 +673,20 @@ def run_profile_case(args):
             o, lse = libattn.fwd(q, k, v, causal=True)
             for _ in range(args.calls):
                 libattn.bwd(q, k, v, o, lse, do, causal=True, deterministic=args.deterministic)
+    elif args.profile_case == "varlen":
+        lens = syn.varlen_lengths(7)
+        cu = torch.from_numpy(syn.cu_seqlens(lens)).cuda()
+        t, mx = int(lens.sum()), int(lens.max())
+        q, k, v, do = (syn.device_normal((t, h, D), bf, 10 + i)
+                       for i, h in enumerate((HQ, HKV, HKV, HQ)))
+        kw = dict(causal=True, window=(256, 0), softcap=50.0)
+        for _ in range(args.calls):
+            o, lse = libattn.fwd_varlen(q, k, v, cu, cu, mx, mx, **kw)
+        for _ in range(args.calls):
+            libattn.bwd_varlen(q, k, v, o, lse, do, cu, cu, mx, mx,
+                               deterministic=args.deterministic, **kw)
     else:
-        b, sq, page = 8, 4, 256
+        b, sq, page = 16, 4, 256
         seqlens, table, npages = syn.decode_layout(9, b, 32768, page, sq)
         kc = syn.device_normal((npages, page, HKV, D), bf, 5)
         vc = syn.device_normal((npages, page, HKV, D), bf, 6)
@@ -693,7 +712,7 @@ def main():
     ap.add_argument("--no-extras", action="store_true", help="skip varlen/decode lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-accuracy", action="store_true", help="skip the oracle error sample")
-    ap.add_argument("--profile-case", choices=["fwd", "bwd", "decode"],
+    ap.add_argument("--profile-case", choices=["fwd", "bwd", "decode", "varlen"],
                     help="run one small fixed case for a profiler capture and exit")
     ap.add_argument("--calls", type=int, default=2, help="calls of --profile-case")
     ap.add_argument("--deterministic", action="store_true", help="--profile-case bwd mode")
