@@ -2,20 +2,27 @@
 //
 // dQ_i = scale * sum_j dS_ij k_j with dS = P * (dP - D), P = exp(s - LSE),
 // dP = dO V^T ("FlashAttention完整说明" §二.2: S and P are recomputed from
-// Q, K and the saved LSE).  A CTA owns two 128-row query tiles of one
-// (batch, head) and walks the 64-key tiles they can see; dQ stays in TMEM
-// for the whole walk and is written once, so no atomics are needed and the
-// result is the same bit for bit on every run (Inference Cookbook FAQ Q11).
+// Q, K and the saved LSE).  A CTA owns one 128-row query tile of one (batch,
+// head) and walks the 128-key tiles it can see; dQ stays in TMEM for the
+// whole walk and is written once, so no atomics are needed and the result is
+// the same bit for bit on every run (Inference Cookbook FAQ Q11).
 //
-//   warpgroup 0   warp 0: TMA (Q, dO of both tiles once; K, V tiles into a
-//                 3-stage ring); warp 1: MMA issuer and TMEM owner.
-//   warpgroups 1, 2   one per query tile, one thread per query row: P and dS
-//                 from S and dP (TMEM), dS (fp16/bf16) written back into the
-//                 S columns as the A operand of dQ += dS K.
+//   warp 0        TMA producer: Q and dO of the tile once; K tiles into a
+//                 3-stage ring, V tiles into a 2-stage ring (a V tile is
+//                 released as soon as its dP product is done, a K tile only
+//                 after its dQ product).
+//   warp 1        MMA issuer and TMEM owner.
+//   warpgroups    one thread per query row; warpgroup w takes keys
+//   1 and 2       [64 w, 64 w + 64) of every key tile: P and dS from S and dP
+//                 (TMEM), dS (fp16/bf16) written back over its own S columns
+//                 as the A operand of dQ += dS K.  At the end warpgroup w
+//                 writes dQ columns [64 w, 64 w + 64).
 //
-// TMEM (512 columns): S_0 [0,64), S_1 [64,128), dP_0 [128,192),
-// dP_1 [192,256), dQ_0 [256,384), dQ_1 [384,512).  The MMA warp alternates
-// between the tiles, so one tile's P/dS work overlaps the other's MMAs.
+// TMEM (512 columns): S of key tile j in buffer j % 2 at [0,128) / [128,256),
+// dP at [256,384), dQ at [384,512).  Issue order: S(0) dP(0) S(1) |
+// dP(j+1) once both warpgroups have read dP(j); dQ(j) once dS(j) is written;
+// S(j+2) into the buffer dQ(j) reads, behind it in issue order.  So while the
+// softmax works on tile j the tensor pipe runs dQ(j-1), S(j+1) and dP(j+1).
 #include <cudaTypedefs.h>
 
 #include "kernels.h"
@@ -26,23 +33,25 @@ namespace {
 using namespace sm103;
 
 constexpr int D = 128;
-constexpr int BM = 128;  // query rows per tile
-constexpr int NT = 2;    // query tiles per CTA
-constexpr int BN = 64;   // keys per step
-constexpr int ST = 3;
+constexpr int BM = 128;  // query rows per CTA
+constexpr int BN = 128;  // keys per step
+constexpr int KST = 3;   // K ring stages
+constexpr int VST = 2;   // V ring stages
 constexpr int kThreads = 384;
-constexpr int kQBytes = BM * D * 2;    // 32 KB, one tile of Q (and of dO)
-constexpr int kKVBytes = BN * D * 2;   // 16 KB
-constexpr int kSmemData = 2 * NT * kQBytes + 2 * ST * kKVBytes;  // 224 KB
+constexpr int kTile = 128 * D * 2;  // 32 KB: one 128-row tile of Q, dO, K or V
+constexpr int kSmemData = 2 * kTile + (KST + VST) * kTile;  // 224 KB
 constexpr int kSmem = kSmemData + 1024;
-constexpr uint32_t kColS = 0, kColDP = 128, kColDQ = 256;
+constexpr uint32_t kColS = 0, kColDP = 256, kColDQ = 384;
 
 struct Shared {
   uint64_t q_full;
-  uint64_t kv_full[ST], kv_empty[ST];
-  uint64_t s_full[NT], ds_full[NT], dq_done[NT];
-  uint64_t all_done;  // every MMA of the CTA has completed
-  uint64_t wait_ns;   // wall-clock limit of a wait
+  uint64_t k_full[KST], k_empty[KST], v_full[VST], v_empty[VST];
+  uint64_t s_full[2];  // S(j) of buffer j % 2 is in TMEM
+  uint64_t dp_full;    // dP(j) is in TMEM
+  uint64_t dp_free;    // both warpgroups have read dP(j)
+  uint64_t ds_full[2]; // dS(j) is written over its S columns
+  uint64_t all_done;   // every MMA of the CTA has completed
+  uint64_t wait_ns;    // wall-clock limit of a wait
   uint32_t tmem_base;
   int abort;
 };
@@ -74,10 +83,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ Shared sh;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
-  uint8_t *q_s = smem;                      // [tile] 32 KB each
-  uint8_t *do_s = smem + NT * kQBytes;      // [tile]
-  uint8_t *k_s = do_s + NT * kQBytes;       // [stage] 16 KB
-  uint8_t *v_s = k_s + ST * kKVBytes;       // [stage]
+  uint8_t *q_s = smem;
+  uint8_t *do_s = smem + kTile;
+  uint8_t *k_s = smem + 2 * kTile;        // [KST]
+  uint8_t *v_s = k_s + KST * kTile;       // [VST]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // CTA -> (query block, batch, head): heaviest blocks first, heads fastest
@@ -87,10 +96,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int mb = m_blocks - 1 - bid / (f.hq * f.batch);
   int q0, lq, k0, lk;
   if (!f.seqs.get(b, q0, lq, k0, lk, f.err)) return;
-  const int m0 = mb * (BM * NT);
+  const int m0 = mb * BM;
   if (m0 >= lq) return;
   const int kvh = h / (f.hq / f.hkv);
-  const int m_last = min(m0 + BM * NT, lq) - 1;
+  const int m_last = min(m0 + BM, lq) - 1;
   int lo_first, hi_first, lo_last, hi_last;
   key_range(m0, lq, lk, f.win_l, f.win_r, lo_first, hi_first);
   key_range(m_last, lq, lk, f.win_l, f.win_r, lo_last, hi_last);
@@ -102,15 +111,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&sh.q_full, 1);
-    for (int s = 0; s < ST; ++s) {
-      mbar_init(&sh.kv_full[s], 1);
-      mbar_init(&sh.kv_empty[s], 1);
+    for (int s = 0; s < KST; ++s) {
+      mbar_init(&sh.k_full[s], 1);
+      mbar_init(&sh.k_empty[s], 1);
     }
-    for (int t = 0; t < NT; ++t) {
-      mbar_init(&sh.s_full[t], 1);
-      mbar_init(&sh.ds_full[t], BM);
-      mbar_init(&sh.dq_done[t], 1);
+    for (int s = 0; s < VST; ++s) {
+      mbar_init(&sh.v_full[s], 1);
+      mbar_init(&sh.v_empty[s], 1);
     }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&sh.s_full[s], 1);
+      mbar_init(&sh.ds_full[s], 8);  // warps
+    }
+    mbar_init(&sh.dp_full, 1);
+    mbar_init(&sh.dp_free, 8);       // warps
     mbar_init(&sh.all_done, 1);
     sh.wait_ns = f.wait_ns;
     sh.abort = 0;
@@ -124,9 +138,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sh.tmem_base;
-  // launched at 168 registers a thread (12 warps); 128 * 112 + 256 * 192 <= 384 * 168
+  // launched at 168 registers a thread (12 warps); 128 * 88 + 256 * 208 = 384 * 168
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 112;" ::: "memory");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;" ::: "memory");
     if (warp == 0) {
       // ---------------------------------------------------------- producer
       if (elect_one() && nt > 0) {
@@ -134,31 +148,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
         prefetch_tmap(&tdo);
-        mbar_expect_tx(&sh.q_full, 2 * NT * kQBytes);
-        for (int t = 0; t < NT; ++t)
-          for (int c = 0; c < D / 64; ++c) {
-            tma_load_3d(q_s + t * kQBytes + c * BM * 128, &tq, &sh.q_full, c * 64, h,
-                        q0 + m0 + t * BM);
-            tma_load_3d(do_s + t * kQBytes + c * BM * 128, &tdo, &sh.q_full, c * 64, h,
-                        q0 + m0 + t * BM);
-          }
-        int issued = 0;
+        mbar_expect_tx(&sh.q_full, 2 * kTile);
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_3d(q_s + c * BM * 128, &tq, &sh.q_full, c * 64, h, q0 + m0);
+          tma_load_3d(do_s + c * BM * 128, &tdo, &sh.q_full, c * 64, h, q0 + m0);
+        }
+        int k_issued = 0, v_issued = 0;
         for (int j = 0; j < nt; ++j) {
-          const int st = j % ST;
           const int krow = k0 + (n_lo + j) * BN;
-          if (!wait_bar(sh, &sh.kv_empty[st], ((j / ST) & 1) ^ 1, f.err)) break;
-          mbar_expect_tx(&sh.kv_full[st], 2 * kKVBytes);
-          for (int c = 0; c < D / 64; ++c) {
-            tma_load_3d(k_s + st * kKVBytes + c * BN * 128, &tk, &sh.kv_full[st], c * 64, kvh, krow);
-            tma_load_3d(v_s + st * kKVBytes + c * BN * 128, &tv, &sh.kv_full[st], c * 64, kvh, krow);
-          }
-          issued = j + 1;
+          const int ks = j % KST, vs = j % VST;
+          if (!wait_bar(sh, &sh.k_empty[ks], ((j / KST) & 1) ^ 1, f.err)) break;
+          mbar_expect_tx(&sh.k_full[ks], kTile);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(k_s + ks * kTile + c * BN * 128, &tk, &sh.k_full[ks], c * 64, kvh, krow);
+          k_issued = j + 1;
+          if (!wait_bar(sh, &sh.v_empty[vs], ((j / VST) & 1) ^ 1, f.err)) break;
+          mbar_expect_tx(&sh.v_full[vs], kTile);
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_3d(v_s + vs * kTile + c * BN * 128, &tv, &sh.v_full[vs], c * 64, kvh, krow);
+          v_issued = j + 1;
         }
         if (*(volatile int *)&sh.abort) {
+          // let this CTA's copies in flight land before the CTA exits
           int *noerr = nullptr;
           mbar_wait(&sh.q_full, 0, noerr);
-          for (int j = max(0, issued - ST); j < issued; ++j)
-            mbar_wait(&sh.kv_full[j % ST], (j / ST) & 1, noerr);
+          for (int j = max(0, k_issued - KST); j < k_issued; ++j)
+            mbar_wait(&sh.k_full[j % KST], (j / KST) & 1, noerr);
+          for (int j = max(0, v_issued - VST); j < v_issued; ++j)
+            mbar_wait(&sh.v_full[j % VST], (j / VST) & 1, noerr);
         }
       }
     } else if (warp == 1) {
@@ -172,52 +189,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t k_d = smem_desc(smem_u32(k_s), 16, 1024);
         const uint64_t v_d = smem_desc(smem_u32(v_s), 16, 1024);
         const uint64_t k_mn = smem_desc(smem_u32(k_s), BN * 128, 1024);
-        auto mma_sdp = [&](int t, int j) {
-          const uint32_t ko = (j % ST) * kKVBytes;
+        // X (Q or dO) times the key tile's K or V rows, K = d
+        auto mma_xk = [&](uint32_t dcol, uint64_t a_d, uint64_t b_d, uint32_t b_off) {
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t qo = t * kQBytes + (kk / 4) * (BM * 128) + (kk % 4) * 32;
-            const uint32_t kvo = ko + (kk / 4) * (BN * 128) + (kk % 4) * 32;
-            mma_ss(tmem + kColS + t * BN, desc_add(q_d, qo), desc_add(k_d, kvo), id_s, kk > 0);
-            mma_ss(tmem + kColDP + t * BN, desc_add(do_d, qo), desc_add(v_d, kvo), id_s, kk > 0);
+            const uint32_t o = (kk / 4) * (128 * 128) + (kk % 4) * 32;
+            mma_ss(dcol, desc_add(a_d, o), desc_add(b_d, b_off + o), id_s, kk > 0);
           }
-          mma_commit(&sh.s_full[t]);
         };
-        auto mma_dq = [&](int t, int j) {
-          const uint32_t ko = (j % ST) * kKVBytes;
-#pragma unroll
-          for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tmem + kColDQ + t * D, tmem + kColS + t * BN + kk * 8,
-                   desc_add(k_mn, ko + kk * 16 * 128), id_q, (j > 0 || kk > 0) ? 1u : 0u);
-          mma_commit(&sh.dq_done[t]);
+        auto k_ready = [&](int j) {
+          const bool r = wait_bar(sh, &sh.k_full[j % KST], (j / KST) & 1, f.err);
+          tc_fence_after();
+          return r;
+        };
+        auto v_ready = [&](int j) {
+          const bool r = wait_bar(sh, &sh.v_full[j % VST], (j / VST) & 1, f.err);
+          tc_fence_after();
+          return r;
+        };
+        auto issue_s = [&](int j) {  // S(j) = Q K_j^T into buffer j % 2
+          mma_xk(tmem + kColS + (j & 1) * 128, q_d, k_d, (j % KST) * kTile);
+          mma_commit(&sh.s_full[j & 1]);
+        };
+        auto issue_dp = [&](int j) {  // dP(j) = dO V_j^T
+          mma_xk(tmem + kColDP, do_d, v_d, (j % VST) * kTile);
+          mma_commit(&sh.dp_full);
+          mma_commit(&sh.v_empty[j % VST]);  // V_j is no longer read
         };
         // test hook: all_done completes only after this thread's last
         // commit, so this wait can only run out
         bool ok = !(f.stall && !wait_bar(sh, &sh.all_done, 0, f.err));
-        ok = ok && wait_bar(sh, &sh.q_full, 0, f.err) && wait_bar(sh, &sh.kv_full[0], 0, f.err);
-        tc_fence_after();
-        if (ok)
-          for (int t = 0; t < NT; ++t) mma_sdp(t, 0);
-        // S_0, dP_0, S_1, dP_1 | dQ_0(j) S_0/dP_0(j+1) dQ_1(j) S_1/dP_1(j+1) | ...
+        ok = ok && wait_bar(sh, &sh.q_full, 0, f.err) && k_ready(0);
+        if (ok) issue_s(0);
+        ok = ok && v_ready(0);
+        if (ok) issue_dp(0);
+        if (ok && nt > 1 && (ok = k_ready(1))) issue_s(1);
         for (int j = 0; ok && j < nt; ++j) {
-          for (int t = 0; t < NT; ++t) {
-            if (!wait_bar(sh, &sh.ds_full[t], j & 1, f.err)) { ok = false; break; }
-            tc_fence_after();
-            mma_dq(t, j);
-            if (t == NT - 1) mma_commit(&sh.kv_empty[j % ST]);
-            if (j + 1 < nt) {
-              if (t == 0) {
-                if (!wait_bar(sh, &sh.kv_full[(j + 1) % ST], ((j + 1) / ST) & 1, f.err)) {
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-              }
-              mma_sdp(t, j + 1);
-            }
+          if (j + 1 < nt) {
+            // dP(j+1) overwrites dP(j): both warpgroups must have read it
+            if (!wait_bar(sh, &sh.dp_free, j & 1, f.err) || !v_ready(j + 1)) break;
+            issue_dp(j + 1);
+          }
+          if (!wait_bar(sh, &sh.ds_full[j & 1], (j >> 1) & 1, f.err)) break;
+          tc_fence_after();
+          // dQ += dS(j) K_j: A = dS (keys 0-63 at the buffer's columns
+          // [0,32), keys 64-127 at [64,96)), B = K_j with d as N
+          const uint32_t sbuf = tmem + kColS + (j & 1) * 128;
+          const uint32_t ko = (j % KST) * kTile;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tmem + kColDQ, sbuf + (kk / 4) * 64 + (kk % 4) * 8,
+                   desc_add(k_mn, ko + kk * 16 * 128), id_q, (j > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&sh.k_empty[j % KST]);  // K_j is no longer read
+          if (j + 2 < nt) {
+            if (!k_ready(j + 2)) break;
+            issue_s(j + 2);  // into the buffer dQ(j) reads: behind it in issue order
           }
         }
-        // after an abort, no MMA may still run when the TMEM is released
+        // completes when every MMA above has; the epilogue reads dQ after it,
+        // and after an abort no MMA may still run when the TMEM is released
         mma_commit(&sh.all_done);
         if (*(volatile int *)&sh.abort) {
           int *noerr = nullptr;
@@ -226,91 +256,108 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 192;" ::: "memory");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 208;" ::: "memory");
     // ------------------------------------------------------------ P, dS
-    const int t = (warp - 4) >> 2;
-    const int r = 32 * (warp & 3) + lane;  // TMEM lane = query row of the tile
-    const int i = m0 + t * BM + r;
+    const int w = (warp - 4) >> 2;          // key half of every tile
+    const int r = 32 * (warp & 3) + lane;   // TMEM lane = query row of the tile
+    const int i = m0 + r;
     const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
     int lo_i, hi_i;
     key_range(i, lq, lk, f.win_l, f.win_r, lo_i, hi_i);
     int lo_tile_max, hi_tile_min, dummy;
-    key_range(m0 + t * BM + BM - 1, lq, lk, f.win_l, f.win_r, lo_tile_max, dummy);
-    key_range(m0 + t * BM, lq, lk, f.win_l, f.win_r, dummy, hi_tile_min);
+    key_range(m_last, lq, lk, f.win_l, f.win_r, lo_tile_max, dummy);
+    key_range(m0, lq, lk, f.win_l, f.win_r, dummy, hi_tile_min);
     const bool valid = i < lq;
     const int64_t li = f.seqs.lse_index(b, h, q0, valid ? i : 0);
-    const float nlse2 = valid ? a.nlse2[li] : 0.f;  // -LSE * log2(e)
+    const float nlse = valid ? a.nlse2[li] : 0.f;  // -LSE * log2(e)
     const float dsum = valid ? a.dsum[li] : 0.f;
     const bool cap = f.softcap > 0.f;
     const float sl2 = f.scale * kLog2e, cap_in = cap ? f.scale / f.softcap : 0.f;
+    const float cap_l2 = f.softcap * kLog2e;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2), nl2 = f2_pack(nlse, nlse), dd2 = f2_pack(dsum, dsum);
+    const uint64_t capx2 = f2_pack(cap_l2, cap_l2);
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      const int key0 = (n_lo + j) * BN;
-      if (!wait_warp(sh, &sh.s_full[t], j & 1, f.err)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t su[BN], du[BN];
-      tmem_ld32(lane_off + tmem + kColS + t * BN, *reinterpret_cast<uint32_t(*)[32]>(su));
-      tmem_ld32(lane_off + tmem + kColS + t * BN + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
-      tmem_ld32(lane_off + tmem + kColDP + t * BN, *reinterpret_cast<uint32_t(*)[32]>(du));
-      tmem_ld32(lane_off + tmem + kColDP + t * BN + 32, *reinterpret_cast<uint32_t(*)[32]>(du + 32));
-      tmem_wait_ld();
-      const bool need_mask = !valid || key0 < lo_tile_max || key0 + BN - 1 > hi_tile_min;
-      uint32_t pk[BN / 2];
-#pragma unroll
-      for (int e = 0; e < BN; e += 2) {
-        float ds[2];
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int col = e + u;
-          const float s = __uint_as_float(su[col]);
-          float p, dcap = 1.f;
-          if (cap) {
-            const float tt = tanh_fast(s * cap_in);
-            p = ex2(fmaf(f.softcap * kLog2e, tt, nlse2));
-            dcap = 1.f - tt * tt;
-          } else {
-            p = ex2(fmaf(s, sl2, nlse2));
-          }
-          if (need_mask) {
-            const int kj = key0 + col;
-            if (!valid || kj < lo_i || kj > hi_i) p = 0.f;
-          }
-          ds[u] = p * (__uint_as_float(du[col]) - dsum) * dcap;
-        }
-        pk[e / 2] = Elem<T>::from_f2(ds[0], ds[1]);
+      const int key0 = (n_lo + j) * BN + 64 * w;  // first key of this warpgroup's half
+      if (!wait_warp(sh, &sh.s_full[j & 1], (j >> 1) & 1, f.err) ||
+          !wait_warp(sh, &sh.dp_full, j & 1, f.err)) {
+        ok = false;
+        break;
       }
-      // dS (16-bit) over the first BN/2 columns of S: the A operand of dQ += dS K
-      tmem_st16(lane_off + tmem + kColS + t * BN, pk);
-      tmem_st16(lane_off + tmem + kColS + t * BN + 16, pk + 16);
+      tc_fence_after();
+      const uint32_t scol = lane_off + tmem + kColS + (j & 1) * 128 + 64 * w;
+      uint32_t su[64], du[64];
+      tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(su));
+      tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
+      tmem_ld32(lane_off + tmem + kColDP + 64 * w, *reinterpret_cast<uint32_t(*)[32]>(du));
+      tmem_ld32(lane_off + tmem + kColDP + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(du + 32));
+      tmem_wait_ld();
+      tc_fence_before();
+      mbar_arrive_warp(&sh.dp_free);  // dP(j+1) may overwrite the dP columns
+      const bool need_mask = !valid || key0 < lo_tile_max || key0 + 63 > hi_tile_min;
+      uint32_t pk[32];
+#pragma unroll
+      for (int q = 0; q < 32; ++q) {
+        const int c = 2 * q;
+        const uint64_t s2 = f2_pack(__uint_as_float(su[c]), __uint_as_float(su[c + 1]));
+        const uint64_t dp2 = f2_pack(__uint_as_float(du[c]), __uint_as_float(du[c + 1]));
+        float t0, t1;
+        uint64_t dcap = 0;
+        if (cap) {
+          // capped score c tanh(s / c); its derivative factor is 1 - tanh^2
+          const float h0 = tanh_fast(__uint_as_float(su[c]) * cap_in);
+          const float h1 = tanh_fast(__uint_as_float(su[c + 1]) * cap_in);
+          f2_unpack(f2_fma(capx2, f2_pack(h0, h1), nl2), t0, t1);
+          dcap = f2_pack(fmaf(-h0, h0, 1.f), fmaf(-h1, h1, 1.f));
+        } else {
+          f2_unpack(f2_fma(s2, sl2x2, nl2), t0, t1);
+        }
+        float p0 = ex2(t0), p1 = ex2(t1);
+        if (need_mask) {
+          const int kj = key0 + c;
+          if (!valid || kj < lo_i || kj > hi_i) p0 = 0.f;
+          if (!valid || kj + 1 < lo_i || kj + 1 > hi_i) p1 = 0.f;
+        }
+        uint64_t ds2 = f2_mul(f2_pack(p0, p1), f2_sub(dp2, dd2));
+        if (cap) ds2 = f2_mul(ds2, dcap);
+        float d0, d1;
+        f2_unpack(ds2, d0, d1);
+        pk[q] = Elem<T>::from_f2(d0, d1);
+      }
+      // dS (16-bit) over the first half of this warpgroup's S columns: the A
+      // operand of dQ += dS K
+      tmem_st16(scol, pk);
+      tmem_st16(scol + 16, pk + 16);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&sh.ds_full[t]);
+      mbar_arrive_warp(&sh.ds_full[j & 1]);
     }
-    // epilogue: dQ = scale * accumulated dS K
-    if (ok && nt > 0) ok = wait_warp(sh, &sh.dq_done[t], (nt - 1) & 1, f.err);
+    // epilogue: dQ = scale * accumulated dS K; warpgroup w writes d columns
+    // [64 w, 64 w + 64)
+    if (ok && nt > 0) ok = wait_warp(sh, &sh.all_done, 0, f.err);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     if (ok) {
       T *row = static_cast<T *>(a.dq) + (int64_t)(q0 + (valid ? i : 0)) * a.dq_rs + (int64_t)h * D;
 #pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
+      for (int c = 2 * w; c < 2 * w + 2; ++c) {
         uint32_t u[32];
         if (nt > 0) {
-          tmem_ld32(lane_off + tmem + kColDQ + t * D + c * 32, u);
+          tmem_ld32(lane_off + tmem + kColDQ + c * 32, u);
           tmem_wait_ld();
         } else {
 #pragma unroll
           for (int e = 0; e < 32; ++e) u[e] = 0u;
         }
-        uint32_t w[16];
+        uint32_t o[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          w[e] = Elem<T>::from_f2(__uint_as_float(u[2 * e]) * f.scale,
+          o[e] = Elem<T>::from_f2(__uint_as_float(u[2 * e]) * f.scale,
                                   __uint_as_float(u[2 * e + 1]) * f.scale);
         if (valid) {
           uint4 *dst = reinterpret_cast<uint4 *>(row + c * 32);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          for (int e = 0; e < 4; ++e) dst[e] = make_uint4(o[4 * e], o[4 * e + 1], o[4 * e + 2], o[4 * e + 3]);
         }
       }
     }
@@ -336,13 +383,13 @@ cudaError_t bwd_dq(const BwdArgs &a, cudaStream_t st) {
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem_once<bwd_dq_kernel<T>>(kSmem);
   if (e != cudaSuccess) return e;
-  const int m_blocks = (f.seqs.sq + BM * NT - 1) / (BM * NT);
+  const int m_blocks = (f.seqs.sq + BM - 1) / BM;
   const int64_t grid = (int64_t)m_blocks * f.hq * f.batch;
   if (grid == 0) return cudaSuccess;
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
-  debug_log("backward dQ (deterministic): bwd_dq_kernel d=128, %d query tiles of %d rows per "
-            "CTA, %d-key tiles, grid=%lld CTAs x %d threads, smem=%d B", NT, BM, BN,
-            (long long)grid, kThreads, kSmem);
+  debug_log("backward dQ (deterministic): bwd_dq_kernel d=128, one %d-row query tile per CTA, "
+            "%d-key steps, grid=%lld CTAs x %d threads, smem=%d B", BM, BN, (long long)grid,
+            kThreads, kSmem);
   bwd_dq_kernel<T><<<(unsigned)grid, kThreads, kSmem, st>>>(tq, tk, tv, tdo, a, m_blocks);
   count_launches(1);
   return cudaGetLastError();
