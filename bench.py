@@ -227,6 +227,45 @@ def bench_varlen(libattn, steps, stream):
             "flops_note": "algorithmic: 4*hq*d*visible pairs (fwd), x2.5 bwd"}
 
 
+def bench_head_dims(libattn, steps, stream):
+    """Forward and backward TFLOP/s at head dims 64 and 256 beside 128, on a
+    causal bf16 problem of the training shape's kind (b=2, s=4096, GQA 4:1,
+    hq * d = 4096): the d = 64 backward runs on the tensor cores like d = 128,
+    the d = 256 backward on the CUDA-core row kernels."""
+    import torch
+
+    out = {}
+    b, s = 2, 4096
+    for d, hq in ((64, 64), (128, 32), (256, 16)):
+        hkv = hq // 4
+        q, do = (dev_normal((b, s, hq, d), 90 + i, torch.bfloat16) for i in range(2))
+        k, v = (dev_normal((b, s, hkv, d), 92 + i, torch.bfloat16) for i in range(2))
+        o, lse = libattn.fwd(q, k, v, causal=True)
+        ws = libattn.bwd_workspace(q, k, False)
+        grads = [torch.empty_like(x) for x in (q, k, v)]
+        flops = 4.0 * b * hq * s * s * d / 2
+
+        def f():
+            libattn.fwd(q, k, v, causal=True, out=o, lse=lse)
+
+        def g():
+            libattn.bwd(q, k, v, o, lse, do, causal=True, workspace=ws, dq=grads[0], dk=grads[1],
+                        dv=grads[2])
+
+        f()
+        g()
+        n_b = steps if d != 256 else 2
+        tf, tb = timed(f, steps, stream), timed(g, n_b, stream)
+        out[f"d{d}"] = {"fwd_ms": round(tf, 4), "fwd_tflops": round(flops / tf / 1e9, 2),
+                        "bwd_ms": round(tb, 4), "bwd_tflops": round(2.5 * flops / tb / 1e9, 2),
+                        "bwd_kernel": "CUDA-core row kernels" if d == 256 else "tensor cores"}
+        del q, do, k, v, o, lse, ws, grads
+        torch.cuda.empty_cache()
+    out["workload"] = ("causal bf16 b=2 s=4096, (hq, d) in {(64, 64), (32, 128), (16, 256)}, "
+                       "hkv = hq / 4")
+    return out
+
+
 def bench_decode(libattn, steps, stream, sq):
     import numpy as np
     import torch
@@ -622,6 +661,8 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.empty_cache()
         out["varlen"] = bench_varlen(libattn, extra_steps, stream)
         torch.cuda.empty_cache()
+        out["head_dims"] = bench_head_dims(libattn, extra_steps, stream)
+        torch.cuda.empty_cache()
         for sq in (1, 4):
             r = bench_decode(libattn, extra_steps, stream, sq)
             r["frac_of_hbm"] = round(r["gbs"] / pk["hbm_gbs"], 4)
@@ -643,7 +684,7 @@ def run_profile_case(args):
 
     fwd / bwd   causal bf16 b=1 s=8192 hq=32 hkv=8 d=128 (`--deterministic`
                 for that backward mode)
-    decode      paged decode b=16, sq=s_new=4, hq=32 hkv=8, caches U[1,32768]
+    decode      paged decode b=16, sq=s_new=4 (--decode-sq), hq=32 hkv=8, caches U[1,32768]
                 in 256-token pages (the workload's per-entry shape; 16 entries
                 make several full waves of splits)
     varlen      the varlen workload (64 sequences U[100,4096], window (256,0),
@@ -686,7 +727,7 @@ def run_profile_case(args):
             libattn.bwd_varlen(q, k, v, o, lse, do, cu, cu, mx, mx,
                                deterministic=args.deterministic, **kw)
     else:
-        b, sq, page = 16, 4, 256
+        b, sq, page = 16, args.decode_sq, 256
         seqlens, table, npages = syn.decode_layout(9, b, 32768, page, sq)
         kc = syn.device_normal((npages, page, HKV, D), bf, 5)
         vc = syn.device_normal((npages, page, HKV, D), bf, 6)
@@ -716,6 +757,7 @@ def main():
                     help="run one small fixed case for a profiler capture and exit")
     ap.add_argument("--calls", type=int, default=2, help="calls of --profile-case")
     ap.add_argument("--deterministic", action="store_true", help="--profile-case bwd mode")
+    ap.add_argument("--decode-sq", type=int, default=4, help="--profile-case decode: sq = s_new")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

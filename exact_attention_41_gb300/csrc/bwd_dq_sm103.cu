@@ -1,4 +1,4 @@
-// dQ of the backward, query-stationary, on the tensor cores (sm_103a), d = 128.
+// dQ of the backward, query-stationary, on the tensor cores (sm_103a), d = 64 or 128.
 //
 // dQ_i = scale * sum_j dS_ij k_j with dS = P * (dP - D), P = exp(s - LSE),
 // dP = dO V^T ("FlashAttention完整说明" §二.2: S and P are recomputed from
@@ -32,16 +32,20 @@ namespace attn {
 namespace {
 using namespace sm103;
 
-constexpr int D = 128;
 constexpr int BM = 128;  // query rows per CTA
 constexpr int BN = 128;  // keys per step
 constexpr int KST = 3;   // K ring stages
 constexpr int VST = 2;   // V ring stages
 constexpr int kThreads = 384;
-constexpr int kTile = 128 * D * 2;  // 32 KB: one 128-row tile of Q, dO, K or V
-constexpr int kSmemData = 2 * kTile + (KST + VST) * kTile;  // 224 KB
-constexpr int kSmem = kSmemData + 1024;
 constexpr uint32_t kColS = 0, kColDP = 256, kColDQ = 384;
+
+// Shared-memory sizes for head dimension D (64 or 128).
+template <int D>
+struct DqCfg {
+  static constexpr int kTile = 128 * D * 2;  // one 128-row tile of Q, dO, K or V: 32 KB at 128
+  static constexpr int kSmemData = 2 * kTile + (KST + VST) * kTile;  // 224 KB at d = 128
+  static constexpr int kSmem = kSmemData + 1024;
+};
 
 struct Shared {
   uint64_t q_full;
@@ -73,11 +77,12 @@ __device__ __forceinline__ bool wait_warp(Shared &sh, uint64_t *bar, uint32_t pa
 template <typename T> struct IsBf16 { static constexpr int v = 0; };
 template <> struct IsBf16<__nv_bfloat16> { static constexpr int v = 1; };
 
-template <typename T>
+template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const BwdArgs a, const int m_blocks) {
+  constexpr int kTile = DqCfg<D>::kTile;
   const FwdArgs &f = a.f;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
@@ -340,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) {
       T *row = static_cast<T *>(a.dq) + (int64_t)(q0 + (valid ? i : 0)) * a.dq_rs + (int64_t)h * D;
 #pragma unroll 1
-      for (int c = 2 * w; c < 2 * w + 2; ++c) {
+      for (int c = w * (D / 64); c < (w + 1) * (D / 64); ++c) {
         uint32_t u[32];
         if (nt > 0) {
           tmem_ld32(lane_off + tmem + kColDQ + c * 32, u);
@@ -367,8 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
-template <typename T>
+template <typename T, int D>
 cudaError_t bwd_dq(const BwdArgs &a, cudaStream_t st) {
+  constexpr int kSmem = DqCfg<D>::kSmem;
   const FwdArgs &f = a.f;
   const int64_t rows_q = f.seqs.cu_q ? f.seqs.total_q : (int64_t)f.batch * f.seqs.sq;
   const int64_t rows_k = f.seqs.cu_k ? f.seqs.total_k : (int64_t)f.batch * f.seqs.sk;
@@ -381,16 +387,16 @@ cudaError_t bwd_dq(const BwdArgs &a, cudaStream_t st) {
       !make_map_3d(&tk, f.k, f.dtype, rows_k, f.hkv, D, BN, f.k_rs) ||
       !make_map_3d(&tv, f.v, f.dtype, rows_k, f.hkv, D, BN, f.v_rs))
     return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_once<bwd_dq_kernel<T>>(kSmem);
+  cudaError_t e = set_smem_once<bwd_dq_kernel<T, D>>(kSmem);
   if (e != cudaSuccess) return e;
   const int m_blocks = (f.seqs.sq + BM - 1) / BM;
   const int64_t grid = (int64_t)m_blocks * f.hq * f.batch;
   if (grid == 0) return cudaSuccess;
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
-  debug_log("backward dQ (deterministic): bwd_dq_kernel d=128, one %d-row query tile per CTA, "
-            "%d-key steps, grid=%lld CTAs x %d threads, smem=%d B", BM, BN, (long long)grid,
+  debug_log("backward dQ (deterministic): bwd_dq_kernel d=%d, one %d-row query tile per CTA, "
+            "%d-key steps, grid=%lld CTAs x %d threads, smem=%d B", D, BM, BN, (long long)grid,
             kThreads, kSmem);
-  bwd_dq_kernel<T><<<(unsigned)grid, kThreads, kSmem, st>>>(tq, tk, tv, tdo, a, m_blocks);
+  bwd_dq_kernel<T, D><<<(unsigned)grid, kThreads, kSmem, st>>>(tq, tk, tv, tdo, a, m_blocks);
   count_launches(1);
   return cudaGetLastError();
 }
@@ -398,8 +404,12 @@ cudaError_t bwd_dq(const BwdArgs &a, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_bwd_dq_tc(const BwdArgs &a, cudaStream_t st) {
-  if (a.f.d != D) return cudaErrorInvalidValue;
-  return a.f.dtype == ATTN_BF16 ? bwd_dq<__nv_bfloat16>(a, st) : bwd_dq<__half>(a, st);
+  const bool bf = a.f.dtype == ATTN_BF16;
+  switch (a.f.d) {
+    case 64: return bf ? bwd_dq<__nv_bfloat16, 64>(a, st) : bwd_dq<__half, 64>(a, st);
+    case 128: return bf ? bwd_dq<__nv_bfloat16, 128>(a, st) : bwd_dq<__half, 128>(a, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace attn

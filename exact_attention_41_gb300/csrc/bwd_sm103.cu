@@ -1,4 +1,4 @@
-// Backward attention on the 5th-generation tensor cores (sm_103a), d = 128.
+// Backward attention on the 5th-generation tensor cores (sm_103a), d = 64 or 128.
 //
 // "FlashAttention完整说明" §二.2: the forward keeps only O and the softmax
 // statistics; the backward recomputes S and P tile by tile from Q, K and the
@@ -49,16 +49,20 @@ namespace attn {
 namespace {
 using namespace sm103;
 
-constexpr int D = 128;
 constexpr int BN = 128;   // keys per CTA
 constexpr int BQ = 64;    // query rows per chunk
 constexpr int ST = 3;     // Q/dO ring stages
 constexpr int kThreads = 512;
-constexpr int kTileK = BN * D * 2;       // 32 KB
-constexpr int kChunk = BQ * D * 2;       // 16 KB
 constexpr int kDS = BN * BQ * 2;         // 16 KB: one 16-bit [key][query] array
-constexpr int kSmemData = 2 * kTileK + ST * 2 * kChunk + 2 * 2 * kDS;  // 224 KB
-constexpr int kSmem = kSmemData + 1024;
+
+// Shared-memory sizes for head dimension D (64 or 128).
+template <int D>
+struct BwdCfg {
+  static constexpr int kTileK = BN * D * 2;  // one K or V tile: 32 KB at d = 128
+  static constexpr int kChunk = BQ * D * 2;  // one Q or dO chunk: 16 KB at d = 128
+  static constexpr int kSmemData = 2 * kTileK + ST * 2 * kChunk + 2 * 2 * kDS;  // 224 KB at 128
+  static constexpr int kSmem = kSmemData + 1024;
+};
 constexpr uint32_t kColDV = 0, kColDK = 128, kColBuf = 256;
 
 struct Shared {
@@ -217,11 +221,12 @@ __device__ __forceinline__ void half_p_ds(uint32_t row_t, uint32_t buf, int hq, 
   tmem_st16(row_t + buf + 32 * hq + 16, pl);
 }
 
-template <typename T>
+template <typename T, int D>
 __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const BwdArgs a, const int n_blocks) {
+  constexpr int kTileK = BwdCfg<D>::kTileK, kChunk = BwdCfg<D>::kChunk;
   const FwdArgs &f = a.f;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
@@ -484,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       T *dvr = static_cast<T *>(a.dv) + (int64_t)(k0 + kj) * a.dv_rs + (int64_t)kvh * D;
       T *dkr = static_cast<T *>(a.dk) + (int64_t)(k0 + kj) * a.dk_rs + (int64_t)kvh * D;
 #pragma unroll 1
-      for (int c = 2 * w; c < 2 * w + 2; ++c) {
+      for (int c = w * (D / 64); c < (w + 1) * (D / 64); ++c) {
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           uint32_t u[32];
@@ -513,6 +518,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
     // ------------------------------------------------------------ dQ
     const int dl = 32 * (warp & 3) + lane;  // TMEM lane = head-dim column
+    // at d = 64 the dQ^T product still has 128 rows (lanes 64-127 hold
+    // nothing of use); those two warps only keep the barrier counts
+    const bool dq_rows = 32 * (warp & 3) < D;
     // the accumulator is (hq, rows, d): a chunk's rows are D floats apart
     const int64_t rows_all = f.seqs.cu_q ? f.seqs.total_q : (int64_t)f.batch * f.seqs.sq;
     for (int it = 0; with_dq && it < n_iter; ++it) {
@@ -523,11 +531,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint32_t u[BQ];
       const uint32_t col = kColBuf + 128 * bf + 64;
-      tmem_ld32(row_t + col, *reinterpret_cast<uint32_t(*)[32]>(u));
-      tmem_ld32(row_t + col + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
-      tmem_wait_ld();
+      if (dq_rows) {
+        tmem_ld32(row_t + col, *reinterpret_cast<uint32_t(*)[32]>(u));
+        tmem_ld32(row_t + col + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+        tmem_wait_ld();
+      }
       tc_fence_before();
       mbar_arrive_relaxed_warp(&sh.dq_free[bf]);  // not behind the previous chunk's adds
+      if (!dq_rows) continue;
       float *acc = a.dq_acc + ((int64_t)h * rows_all + q0 + i0) * D + dl;
       const int rows = min(BQ, lq - i0);
 #pragma unroll
@@ -542,8 +553,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // (LSE_i * log2(e), D_i = rowsum(dO_i * O_i)) per row (fp32, LSE layout);
 // zero the dQ accumulator of the atomic mode.  One warp per (row, head).
-template <typename T>
+template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int64_t rows) {
+  constexpr int V = D / 32;  // values per lane
   const FwdArgs &f = a.f;
   const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -551,14 +563,18 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int64_t rows) 
   for (int64_t x = w; x < rows * f.hq; x += nw) {
     const int64_t row = x / f.hq;
     const int h = (int)(x % f.hq);
-    const int64_t off = x * D + lane * 4;
-    float o[4], g[4];
-    load_vec<T, 4>(static_cast<const T *>(f.o) + off, o);
-    load_vec<T, 4>(static_cast<const T *>(a.dout) + off, g);
-    float s = o[0] * g[0] + o[1] * g[1] + o[2] * g[2] + o[3] * g[3];
+    const int64_t off = x * D + lane * V;
+    float o[V], g[V];
+    load_vec<T, V>(static_cast<const T *>(f.o) + off, o);
+    load_vec<T, V>(static_cast<const T *>(a.dout) + off, g);
+    float s = 0.f;
+#pragma unroll
+    for (int e = 0; e < V; ++e) s = fmaf(o[e], g[e], s);
     s = warp_sum(s);
-    if (!a.deterministic)
-      reinterpret_cast<float4 *>(a.dq_acc + off)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (!a.deterministic) {
+#pragma unroll
+      for (int e = 0; e < V; ++e) a.dq_acc[off + e] = 0.f;
+    }
     if (lane == 0) {
       int64_t li;
       if (f.seqs.cu_q) {
@@ -575,7 +591,7 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int64_t rows) 
 
 // dQ = scale * dQ_acc -> dtype: the accumulator is (hq, rows, d), dQ
 // (rows, hq, d) with rows dq_rs elements apart.  One thread per 4 values.
-template <typename T>
+template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdArgs a, int64_t rows, int64_t n4) {
   const int hq = a.f.hq;
   for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n4;
@@ -593,14 +609,15 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdArgs a, int64_t 
   }
 }
 
-template <typename T>
+template <typename T, int D>
 cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
+  constexpr int kSmem = BwdCfg<D>::kSmem;
   const FwdArgs &f = a.f;
   const int64_t rows_q = f.seqs.cu_q ? f.seqs.total_q : (int64_t)f.batch * f.seqs.sq;
   const int64_t rows_k = f.seqs.cu_k ? f.seqs.total_k : (int64_t)f.batch * f.seqs.sk;
   const int prep_blocks = (int)std::min<int64_t>((rows_q * f.hq + 7) / 8, (int64_t)sms * 16);
   if (rows_q > 0) {
-    bwd_prep_kernel<T><<<std::max(prep_blocks, 1), 256, 0, st>>>(a, rows_q);
+    bwd_prep_kernel<T, D><<<std::max(prep_blocks, 1), 256, 0, st>>>(a, rows_q);
     count_launches(1);
   }
   if (rows_k > 0 && rows_q > 0) {
@@ -610,16 +627,16 @@ cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
         !make_map_3d(&tk, f.k, f.dtype, rows_k, f.hkv, D, BN, f.k_rs) ||
         !make_map_3d(&tv, f.v, f.dtype, rows_k, f.hkv, D, BN, f.v_rs))
       return cudaErrorInvalidValue;
-    cudaError_t e = set_smem_once<bwd_tc_kernel<T>>(kSmem);
+    cudaError_t e = set_smem_once<bwd_tc_kernel<T, D>>(kSmem);
     if (e != cudaSuccess) return e;
     const int n_blocks = (f.seqs.sk + BN - 1) / BN;
     const int64_t grid = (int64_t)n_blocks * f.hkv * f.batch;
     if (grid > INT32_MAX) return cudaErrorInvalidValue;
-    debug_log("backward: bwd_tc_kernel d=128, %d keys per CTA, %d-query chunks, dQ %s, "
-              "grid=%lld CTAs x %d threads, smem=%d B", BN, BQ,
+    debug_log("backward: bwd_tc_kernel d=%d, %d keys per CTA, %d-query chunks, dQ %s, "
+              "grid=%lld CTAs x %d threads, smem=%d B", D, BN, BQ,
               a.deterministic ? "by the query-stationary kernel (deterministic)" : "atomic fp32 adds",
               (long long)grid, kThreads, kSmem);
-    bwd_tc_kernel<T><<<(unsigned)grid, kThreads, kSmem, st>>>(tq, tk, tv, tdo, a, n_blocks);
+    bwd_tc_kernel<T, D><<<(unsigned)grid, kThreads, kSmem, st>>>(tq, tk, tv, tdo, a, n_blocks);
     count_launches(1);
   } else if (rows_k > 0) {  // no queries: the key gradients are zero
     const size_t w = (size_t)f.hkv * D * 2;
@@ -634,7 +651,7 @@ cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
   } else if (rows_q > 0) {
     const int64_t n4 = rows_q * f.hq * D / 4;
     const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, (int64_t)sms * 16);
-    bwd_dq_convert_kernel<T><<<std::max(blocks, 1), 256, 0, st>>>(a, rows_q, n4);
+    bwd_dq_convert_kernel<T, D><<<std::max(blocks, 1), 256, 0, st>>>(a, rows_q, n4);
     count_launches(1);
   }
   return cudaGetLastError();
@@ -643,9 +660,12 @@ cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
 }  // namespace
 
 cudaError_t launch_bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
-  if (a.f.d != D) return cudaErrorInvalidValue;
-  return a.f.dtype == ATTN_BF16 ? bwd_tc<__nv_bfloat16>(a, sms, st)
-                                : bwd_tc<__half>(a, sms, st);
+  const bool bf = a.f.dtype == ATTN_BF16;
+  switch (a.f.d) {
+    case 64: return bf ? bwd_tc<__nv_bfloat16, 64>(a, sms, st) : bwd_tc<__half, 64>(a, sms, st);
+    case 128: return bf ? bwd_tc<__nv_bfloat16, 128>(a, sms, st) : bwd_tc<__half, 128>(a, sms, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace attn
