@@ -230,8 +230,8 @@ def bench_varlen(libattn, steps, stream):
 def bench_head_dims(libattn, steps, stream):
     """Forward and backward TFLOP/s at head dims 64 and 256 beside 128, on a
     causal bf16 problem of the training shape's kind (b=2, s=4096, GQA 4:1,
-    hq * d = 4096): the d = 64 backward runs on the tensor cores like d = 128,
-    the d = 256 backward on the CUDA-core row kernels."""
+    hq * d = 4096), both dQ modes.  Every backward runs on the tensor cores;
+    at d = 256 the deterministic dQ comes from the row kernel."""
     import torch
 
     out = {}
@@ -242,24 +242,27 @@ def bench_head_dims(libattn, steps, stream):
         k, v = (dev_normal((b, s, hkv, d), 92 + i, torch.bfloat16) for i in range(2))
         o, lse = libattn.fwd(q, k, v, causal=True)
         ws = libattn.bwd_workspace(q, k, False)
+        ws_det = libattn.bwd_workspace(q, k, True)
         grads = [torch.empty_like(x) for x in (q, k, v)]
         flops = 4.0 * b * hq * s * s * d / 2
 
         def f():
             libattn.fwd(q, k, v, causal=True, out=o, lse=lse)
 
-        def g():
-            libattn.bwd(q, k, v, o, lse, do, causal=True, workspace=ws, dq=grads[0], dk=grads[1],
-                        dv=grads[2])
+        def g(det=False):
+            libattn.bwd(q, k, v, o, lse, do, causal=True, deterministic=det,
+                        workspace=ws_det if det else ws, dq=grads[0], dk=grads[1], dv=grads[2])
 
         f()
         g()
-        n_b = steps if d != 256 else 2
-        tf, tb = timed(f, steps, stream), timed(g, n_b, stream)
+        g(True)
+        tf, tb = timed(f, steps, stream), timed(g, steps, stream)
+        td = timed(lambda: g(True), steps if d != 256 else 2, stream)
         out[f"d{d}"] = {"fwd_ms": round(tf, 4), "fwd_tflops": round(flops / tf / 1e9, 2),
                         "bwd_ms": round(tb, 4), "bwd_tflops": round(2.5 * flops / tb / 1e9, 2),
-                        "bwd_kernel": "CUDA-core row kernels" if d == 256 else "tensor cores"}
-        del q, do, k, v, o, lse, ws, grads
+                        "bwd_deterministic_ms": round(td, 4),
+                        "bwd_deterministic_tflops": round(2.5 * flops / td / 1e9, 2)}
+        del q, do, k, v, o, lse, ws, ws_det, grads
         torch.cuda.empty_cache()
     out["workload"] = ("causal bf16 b=2 s=4096, (hq, d) in {(64, 64), (32, 128), (16, 256)}, "
                        "hkv = hq / 4")

@@ -124,9 +124,7 @@ attn_status run_bwd(BwdArgs &a, int64_t rows, void *workspace, const DeviceInfo 
   a.dq_acc = a.deterministic ? nullptr : reinterpret_cast<float *>(ws);
   a.f.wait_ns = wait_limit_ns();
   a.f.stall = test_stall();
-  // tensor cores for d = 64 and 128; the CUDA-core row kernels for d = 256
-  if (a.f.d != 256) return launched(launch_bwd_tc(a, di->sms, stream));
-  return launched(launch_bwd_simt(a, stream));
+  return launched(launch_bwd_tc(a, di->sms, stream));
 }
 
 int resolve_splits(int b, int hkv, int max_seqlen_k, int num_splits, int sms) {

@@ -1,4 +1,5 @@
-// Backward attention on the 5th-generation tensor cores (sm_103a), d = 64 or 128.
+// Backward attention on the 5th-generation tensor cores (sm_103a), d = 64, 128
+// or 256.
 //
 // "FlashAttention完整说明" §二.2: the forward keeps only O and the softmax
 // statistics; the backward recomputes S and P tile by tile from Q, K and the
@@ -37,6 +38,15 @@
 // S^T, then P^T high/low, in [0,64); dP^T, then dQ^T, in [64,128).  The MMAs
 // of one thread run in issue order, so the products that read P^T from a
 // buffer finish before the next S^T overwrites it.
+//
+// d = 256 keeps this structure with three changes that make it fit.  Each
+// CTA produces one 128-column half of dK, dV and dQ (two CTAs per key
+// block, each recomputing S and dP over all 256 columns), so dV and dK stay
+// at 128 TMEM columns.  Chunks are 32 queries (buffers of 64 columns; the
+// dS^T arrays have 64-byte rows in the 64-byte swizzle), and the Q/dO ring
+// has 2 stages, so K and V (64 KB each), the ring and dS fit in 224 KB;
+// with 2 stages S^T of chunk it+2 is issued after dK of chunk it, which
+// frees the stage it loads into.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -50,21 +60,28 @@ namespace {
 using namespace sm103;
 
 constexpr int BN = 128;   // keys per CTA
-constexpr int BQ = 64;    // query rows per chunk
-constexpr int ST = 3;     // Q/dO ring stages
 constexpr int kThreads = 512;
-constexpr int kDS = BN * BQ * 2;         // 16 KB: one 16-bit [key][query] array
 
-// Shared-memory sizes for head dimension D (64 or 128).
+// Tile shape for head dimension D (64, 128 or 256).
 template <int D>
 struct BwdCfg {
-  static constexpr int kTileK = BN * D * 2;  // one K or V tile: 32 KB at d = 128
-  static constexpr int kChunk = BQ * D * 2;  // one Q or dO chunk: 16 KB at d = 128
-  static constexpr int kSmemData = 2 * kTileK + ST * 2 * kChunk + 2 * 2 * kDS;  // 224 KB at 128
+  static constexpr int BQ = D == 256 ? 32 : 64;  // query rows per chunk
+  static constexpr int QH = BQ / 2;              // queries of a softmax thread
+  static constexpr int ST = D == 256 ? 2 : 3;    // Q/dO ring stages
+  static constexpr int DO = D < 128 ? D : 128;   // dK/dV/dQ columns of one CTA
+  static constexpr int NH = D / DO;              // CTAs per key block
+  static constexpr int kTileK = BN * D * 2;      // one K or V tile: 32 KB at d = 128
+  static constexpr int kChunk = BQ * D * 2;      // one Q or dO chunk: 16 KB at d = 128
+  static constexpr int kDsRow = BQ * 2;          // bytes per key row of a dS^T array
+  static constexpr int kDS = BN * kDsRow;        // one 16-bit [key][query] array
+  static constexpr uint32_t kDsSwizzle = BQ == 64 ? 2 : 4;  // descriptor: 128- / 64-byte swizzle
+  static constexpr int kSmemData = 2 * kTileK + ST * 2 * kChunk + 2 * 2 * kDS;  // 224 KB
   static constexpr int kSmem = kSmemData + 1024;
+  static_assert(kSmem <= 227 * 1024 - 1024, "shared memory");
 };
 constexpr uint32_t kColDV = 0, kColDK = 128, kColBuf = 256;
 
+template <int ST, int BQ>
 struct Shared {
   uint64_t kv_full;
   uint64_t qd_full[ST], qd_empty[ST];
@@ -87,13 +104,15 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ bool wait_bar(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
+template <typename Sh>
+__device__ __forceinline__ bool wait_bar(Sh &sh, uint64_t *bar, uint32_t parity, int *err) {
   return mbar_wait_bounded(smem_u32(bar), parity, &sh.abort, err, sh.wait_ns);
 }
 
 // The same wait taken by a whole warp with one answer, so warp-collective
 // tcgen05 loads/stores that follow are never reached by part of a warp.
-__device__ __forceinline__ bool wait_warp(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
+template <typename Sh>
+__device__ __forceinline__ bool wait_warp(Sh &sh, uint64_t *bar, uint32_t parity, int *err) {
   return __all_sync(0xffffffffu, wait_bar(sh, bar, parity, err));
 }
 
@@ -128,7 +147,8 @@ __device__ __forceinline__ void split_hi_lo(uint64_t x2, uint32_t &hi, uint32_t 
   lo = Elem<T>::from_f2(l0, l1);
 }
 
-// Query chunks [c_lo, c_lo + nch) that can see any key of block nb.
+// Query chunks [c_lo, c_lo + nch) of BQ rows that can see any key of block nb.
+template <int BQ>
 __device__ __forceinline__ void chunk_range(int nb, int lq, int lk, int win_l, int win_r,
                                             int &c_lo, int &nch) {
   const int key0 = nb * BN, key1 = min(key0 + BN, lk) - 1;
@@ -185,40 +205,55 @@ __device__ __forceinline__ void p_ds_16(const uint32_t *su, const uint32_t *du, 
   }
 }
 
+// Byte offset of 16-byte chunk `c` of row j in a swizzled [row][16-bit]
+// array with `row_bytes`-byte rows: the 128-byte swizzle XORs the chunk
+// index with (row mod 8), the 64-byte one with ((row / 2) mod 4).
+template <int row_bytes>
+__device__ __forceinline__ uint32_t swz_off(int j, int c) {
+  if constexpr (row_bytes == 128) return j * 128 + ((c ^ (j & 7)) << 4);
+  else return j * 64 + ((c ^ ((j >> 1) & 3)) << 4);
+}
+
 // Half a chunk of one softmax thread (key row j; row_t = TMEM base + its
-// lane): the 32 queries [32 hq, 32 hq + 32) of the chunk in buffer `buf`.
-// P^T high/low go back over the S^T columns just read (high at 32 hq +
-// [0,16), low at 32 hq + [16,32)); dS^T high/low into the two [key][query]
-// arrays at ds_hi / ds_hi + kDS.
-template <typename T, bool kCap>
+// lane): the QH = BQ/2 queries [QH hq, QH hq + QH) of the chunk in buffer
+// `buf` (S^T at [0, BQ), dP^T at [BQ, 2 BQ)).  P^T high/low go back over the
+// S^T columns just read (high at QH hq + [0, QH/2), low at QH hq + [QH/2,
+// QH)); dS^T high/low into the two [key][query] arrays at ds_hi and
+// ds_hi + kDS.
+template <typename T, bool kCap, typename C>
 __device__ __forceinline__ void half_p_ds(uint32_t row_t, uint32_t buf, int hq, uint8_t *ds_hi,
                                           int j, const float4 *lsd4, int i0, int qlo, int qhi,
                                           float sl2, float cap_in, float cap_l2) {
-  uint32_t su[32], du[32];
-  tmem_ld32(row_t + buf + 32 * hq, su);
-  tmem_ld32(row_t + buf + 64 + 32 * hq, du);
+  constexpr int QH = C::QH;
+  uint32_t su[QH], du[QH];
+  if constexpr (QH == 32) {
+    tmem_ld32(row_t + buf + 32 * hq, *reinterpret_cast<uint32_t(*)[32]>(su));
+    tmem_ld32(row_t + buf + C::BQ + 32 * hq, *reinterpret_cast<uint32_t(*)[32]>(du));
+  } else {
+    tmem_ld16(row_t + buf + QH * hq, su);
+    tmem_ld16(row_t + buf + C::BQ + QH * hq, du);
+  }
   tmem_wait_ld();
-  const bool masked = i0 < qlo || i0 + 31 > qhi;
-  uint32_t ph[16], pl[16];
+  const bool masked = i0 < qlo || i0 + QH - 1 > qhi;
+  uint32_t pp[QH];  // P^T high parts in [0, QH/2), low parts in [QH/2, QH)
 #pragma unroll
-  for (int hv = 0; hv < 2; ++hv) {
+  for (int hv = 0; hv < QH / 16; ++hv) {
     const int c0 = 16 * hv;
     uint32_t dh[8], dl[8];
     p_ds_16<T, kCap>(su + c0, du + c0, lsd4 + c0 / 2, i0 + c0, qlo, qhi, masked, sl2, cap_in, cap_l2,
-                     ph + 8 * hv, pl + 8 * hv, dh, dl);
-    // dS^T: 16 queries = two 16-byte chunks of the row's 128 bytes
+                     pp + 8 * hv, pp + QH / 2 + 8 * hv, dh, dl);
+    // dS^T: 16 queries = two 16-byte chunks of the key's row
 #pragma unroll
     for (int cc = 0; cc < 2; ++cc) {
-      const int chunk = 4 * hq + 2 * hv + cc;
-      const uint32_t off = j * 128 + ((chunk ^ (j & 7)) << 4);
+      const uint32_t off = swz_off<C::kDsRow>(j, (QH * hq + c0) / 8 + cc);
       *reinterpret_cast<uint4 *>(ds_hi + off) =
           make_uint4(dh[4 * cc], dh[4 * cc + 1], dh[4 * cc + 2], dh[4 * cc + 3]);
-      *reinterpret_cast<uint4 *>(ds_hi + kDS + off) =
+      *reinterpret_cast<uint4 *>(ds_hi + C::kDS + off) =
           make_uint4(dl[4 * cc], dl[4 * cc + 1], dl[4 * cc + 2], dl[4 * cc + 3]);
     }
   }
-  tmem_st16(row_t + buf + 32 * hq, ph);
-  tmem_st16(row_t + buf + 32 * hq + 16, pl);
+#pragma unroll
+  for (int x = 0; x < QH / 16; ++x) tmem_st16(row_t + buf + QH * hq + 16 * x, pp + 16 * x);
 }
 
 template <typename T, int D>
@@ -226,10 +261,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const BwdArgs a, const int n_blocks) {
-  constexpr int kTileK = BwdCfg<D>::kTileK, kChunk = BwdCfg<D>::kChunk;
+  using C = BwdCfg<D>;
+  constexpr int kTileK = C::kTileK, kChunk = C::kChunk, kDS = C::kDS;
+  constexpr int BQ = C::BQ, QH = C::QH, ST = C::ST, DO = C::DO;
   const FwdArgs &f = a.f;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ Shared sh;
+  __shared__ Shared<ST, BQ> sh;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   uint8_t *k_s = smem;
@@ -238,10 +275,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *ds_s = qd_s + ST * 2 * kChunk;      // [buffer][dS high | dS low], each [key][query]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // CTA -> (key block, kv head, batch): key blocks fastest, so the CTAs of one
-  // (batch, kv head) run together and share Q/dO in L2; lower key blocks (the
-  // heaviest under a causal mask) are dispatched first.
-  const int bid = blockIdx.x;
+  // CTA -> (column half, key block, kv head, batch): halves, then key blocks
+  // fastest, so the CTAs of one (batch, kv head) run together and share
+  // Q/dO in L2; lower key blocks (the heaviest under a causal mask) are
+  // dispatched first.  dh selects the head-dim columns [dh DO, dh DO + DO)
+  // of dK, dV and dQ this CTA produces (always 0 below d = 256).
+  const int dh = blockIdx.x % C::NH;
+  const int bid = blockIdx.x / C::NH;
   const int nb = bid % n_blocks;
   const int kvh = (bid / n_blocks) % f.hkv;
   const int b = bid / (n_blocks * f.hkv);
@@ -251,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (key0 >= lk) return;
   const int g = f.hq / f.hkv;
   int c_lo, nch;
-  chunk_range(nb, lq, lk, f.win_l, f.win_r, c_lo, nch);
+  chunk_range<BQ>(nb, lq, lk, f.win_l, f.win_r, c_lo, nch);
   const int n_iter = g * nch;
   // deterministic mode: dQ comes from the query-stationary kernel instead
   const bool with_dq = !a.deterministic;
@@ -345,20 +385,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (elect_one() && n_iter > 0) {
         constexpr int ab = IsBf16<T>::v;
         constexpr uint32_t id_s = idesc_f16(128, BQ, ab, 0, 0);   // S^T, dP^T
-        constexpr uint32_t id_kv = idesc_f16(128, D, ab, 0, 1);   // dV, dK (B = dO/Q, MN-major)
+        constexpr uint32_t id_kv = idesc_f16(128, DO, ab, 0, 1);  // dV, dK (B = dO/Q, MN-major)
         constexpr uint32_t id_q = idesc_f16(128, BQ, ab, 1, 1);   // dQ^T (A = K^T, B = dS^T)
         const uint32_t k_addr = smem_u32(k_s), v_addr = smem_u32(v_s);
         const uint32_t qd_addr = smem_u32(qd_s), ds_addr = smem_u32(ds_s);
         // descriptor bases; every operand below is base + constant offset
         const uint64_t k_kd = smem_desc(k_addr, 16, 1024), v_kd = smem_desc(v_addr, 16, 1024);
-        const uint64_t k_mn = smem_desc(k_addr, BN * 128, 1024);
-        const uint64_t qd_k = smem_desc(qd_addr, 16, 1024), qd_mn = smem_desc(qd_addr, BQ * 128, 1024);
-        const uint64_t ds_k = smem_desc(ds_addr, 16, 1024), ds_mn = smem_desc(ds_addr, BQ * 128, 1024);
+        // the MN-major views start at this CTA's column half (64-column blocks 2 dh, 2 dh + 1)
+        const uint64_t k_mn = smem_desc(k_addr + dh * 2 * (BN * 128), BN * 128, 1024);
+        const uint64_t qd_k = smem_desc(qd_addr, 16, 1024);
+        const uint64_t qd_mn = smem_desc(qd_addr + dh * 2 * (BQ * 128), BQ * 128, 1024);
+        // dS^T arrays: rows of BQ queries, 8-row groups 8 * kDsRow bytes apart
+        const uint64_t ds_k = smem_desc(ds_addr, 16, 8 * C::kDsRow, C::kDsSwizzle);
+        const uint64_t ds_mn = smem_desc(ds_addr, 8 * C::kDsRow, 8 * C::kDsRow, C::kDsSwizzle);
         // S^T = K Q^T (which = 0) or dP^T = V dO^T (which = 1) of chunk `it`
         // into its buffer; the Q/dO stage must have landed
         auto issue_s_or_dp = [&](int it, int which) {
           const int st = it % ST;
-          const uint32_t buf = tmem + kColBuf + 128 * (it & 1) + 64 * which;
+          const uint32_t buf = tmem + kColBuf + 2 * BQ * (it & 1) + BQ * which;
           const uint64_t a_d = which ? v_kd : k_kd;
           const uint32_t b_o = st * 2 * kChunk + which * kChunk;
 #pragma unroll
@@ -385,11 +429,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // S/dP(0) S/dP(1) | dQ(it) dV(it) S(it+2) dK(it) dP(it+2) | ...
         // S(it+2) needs only dV(it) to have read P^T(it) (issue order);
-        // dP(it+2) waits until dQ^T(it) has left the dP^T columns.
+        // dP(it+2) waits until dQ^T(it) has left the dP^T columns.  With a
+        // 2-stage ring, S(it+2) comes after dK(it), whose completion frees
+        // the stage chunk it+2 is loaded into.
         for (int it = 0; ok && it < n_iter; ++it) {
           const int bf = it & 1, st = it % ST;
           const uint32_t par = (it >> 1) & 1;
-          const uint32_t buf = tmem + kColBuf + 128 * bf;
+          const uint32_t buf = tmem + kColBuf + 2 * BQ * bf;
           const uint32_t dso = bf * 2 * kDS;
           if (!wait_bar(sh, &sh.pds_full[bf], par, f.err)) break;
           tc_fence_after();
@@ -397,8 +443,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // dQ^T = K^T dS^T (high part) into the dP^T columns, already read
 #pragma unroll
             for (int kk = 0; kk < BN / 16; ++kk)
-              mma_ss(buf + 64, desc_add(k_mn, kk * 16 * 128), desc_add(ds_mn, dso + kk * 16 * 128),
-                     id_q, kk > 0);
+              mma_ss(buf + BQ, desc_add(k_mn, kk * 16 * 128),
+                     desc_add(ds_mn, dso + kk * 16 * C::kDsRow), id_q, kk > 0);
             mma_commit(&sh.dq_full[bf]);
           }
           const uint32_t q_o = st * 2 * kChunk, do_o = q_o + kChunk;
@@ -407,14 +453,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             // dV += (P_high + P_low)^T dO
             const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
             const uint64_t do_d = desc_add(qd_mn, do_o + kk * 16 * 128);
-            const uint32_t pc = buf + (kk / 2) * 32 + (kk % 2) * 8;
+            // queries 16 kk.. of the chunk: softmax half 16 kk / QH, its
+            // 16-query step (16 kk % QH) / 16; low parts QH / 2 columns on
+            const uint32_t pc = buf + QH * (16 * kk / QH) + 8 * ((16 * kk % QH) / 16);
             mma_ts(tmem + kColDV, pc, do_d, id_kv, acc);
-            mma_ts(tmem + kColDV, pc + 16, do_d, id_kv, 1u);
+            mma_ts(tmem + kColDV, pc + QH / 2, do_d, id_kv, 1u);
           }
           const bool next = it + 2 < n_iter;
-          if (next) {
-            if (!stage_ready(it + 2)) break;
-            issue_s_or_dp(it + 2, 0);
+          if constexpr (ST >= 3) {
+            if (next) {
+              if (!stage_ready(it + 2)) break;
+              issue_s_or_dp(it + 2, 0);
+            }
           }
 #pragma unroll
           for (int kk = 0; kk < BQ / 16; ++kk) {
@@ -426,6 +476,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(&sh.qd_empty[st]);  // Q and dO of this chunk are no longer read
           if (next) {
+            if constexpr (ST < 3) {
+              if (!stage_ready(it + 2)) break;
+              issue_s_or_dp(it + 2, 0);
+            }
             if (with_dq && !wait_bar(sh, &sh.dq_free[bf], par, f.err)) break;
             tc_fence_after();
             issue_s_or_dp(it + 2, 1);
@@ -444,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < 12) {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 152;" ::: "memory");
     // ------------------------------------------------------------ P^T, dS^T
-    const int w = (warp - 4) >> 2;          // which half of every chunk's 64 queries
+    const int w = (warp - 4) >> 2;          // which half of every chunk's queries
     const int j = 32 * (warp & 3) + lane;  // TMEM lane = key row of the block
     const int kj = key0 + j;
     int qlo, qhi;
@@ -457,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = 0; it < n_iter; ++it) {
       const int bf = it & 1, st = it % ST;
       const uint32_t par = (it >> 1) & 1;
-      const int i0 = (c_lo + it % nch) * BQ + 32 * w;
+      const int i0 = (c_lo + it % nch) * BQ + QH * w;
       // S^T, dP^T of this chunk; the commit behind it also covers the MMAs of
       // this buffer's previous chunk, so its dS^T arrays are free.  The
       // stage's (LSE, D) copies landed before its S^T was computed; the wait
@@ -469,27 +523,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       uint8_t *ds_hi = ds_s + bf * 2 * kDS;
-      const uint32_t buf = kColBuf + 128 * bf;
-      const float4 *lsd4 = reinterpret_cast<const float4 *>(sh.lsd[st]) + 16 * w;
+      const uint32_t buf = kColBuf + 2 * BQ * bf;
+      const float4 *lsd4 = reinterpret_cast<const float4 *>(sh.lsd[st]) + (QH / 2) * w;
       if (cap)
-        half_p_ds<T, true>(row_t, buf, w, ds_hi, j, lsd4, i0, qlo, qhi, sl2, cap_in, cap_l2);
+        half_p_ds<T, true, C>(row_t, buf, w, ds_hi, j, lsd4, i0, qlo, qhi, sl2, cap_in, cap_l2);
       else
-        half_p_ds<T, false>(row_t, buf, w, ds_hi, j, lsd4, i0, qlo, qhi, sl2, cap_in, cap_l2);
+        half_p_ds<T, false, C>(row_t, buf, w, ds_hi, j, lsd4, i0, qlo, qhi, sl2, cap_in, cap_l2);
       tmem_wait_st();
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       tc_fence_before();
       mbar_arrive_warp(&sh.pds_full[bf]);
     }
-    // dK, dV out of TMEM: each warpgroup writes half of the head-dim columns
+    // dK, dV out of TMEM: each warpgroup writes half of this CTA's columns
     if (ok && n_iter > 0) ok = wait_warp(sh, &sh.all_done, 0, f.err);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     // tcgen05.ld is warp-collective: every lane loads, only real keys store
     if (ok) {
-      T *dvr = static_cast<T *>(a.dv) + (int64_t)(k0 + kj) * a.dv_rs + (int64_t)kvh * D;
-      T *dkr = static_cast<T *>(a.dk) + (int64_t)(k0 + kj) * a.dk_rs + (int64_t)kvh * D;
+      const int64_t col0 = (int64_t)kvh * D + dh * DO;
+      T *dvr = static_cast<T *>(a.dv) + (int64_t)(k0 + kj) * a.dv_rs + col0;
+      T *dkr = static_cast<T *>(a.dk) + (int64_t)(k0 + kj) * a.dk_rs + col0;
 #pragma unroll 1
-      for (int c = w * (D / 64); c < (w + 1) * (D / 64); ++c) {
+      for (int c = w * (DO / 64); c < (w + 1) * (DO / 64); ++c) {
 #pragma unroll
         for (int which = 0; which < 2; ++which) {
           uint32_t u[32];
@@ -517,10 +572,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 104;" ::: "memory");
     // ------------------------------------------------------------ dQ
-    const int dl = 32 * (warp & 3) + lane;  // TMEM lane = head-dim column
+    const int dl = 32 * (warp & 3) + lane;  // TMEM lane = column dh DO + dl
     // at d = 64 the dQ^T product still has 128 rows (lanes 64-127 hold
     // nothing of use); those two warps only keep the barrier counts
-    const bool dq_rows = 32 * (warp & 3) < D;
+    const bool dq_rows = 32 * (warp & 3) < DO;
     // the accumulator is (hq, rows, d): a chunk's rows are D floats apart
     const int64_t rows_all = f.seqs.cu_q ? f.seqs.total_q : (int64_t)f.batch * f.seqs.sq;
     for (int it = 0; with_dq && it < n_iter; ++it) {
@@ -530,16 +585,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!wait_warp(sh, &sh.dq_full[bf], (it >> 1) & 1, f.err)) break;
       tc_fence_after();
       uint32_t u[BQ];
-      const uint32_t col = kColBuf + 128 * bf + 64;
+      const uint32_t col = kColBuf + 2 * BQ * bf + BQ;
       if (dq_rows) {
-        tmem_ld32(row_t + col, *reinterpret_cast<uint32_t(*)[32]>(u));
-        tmem_ld32(row_t + col + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+#pragma unroll
+        for (int x = 0; x < BQ / 32; ++x)
+          tmem_ld32(row_t + col + 32 * x, *reinterpret_cast<uint32_t(*)[32]>(u + 32 * x));
         tmem_wait_ld();
       }
       tc_fence_before();
       mbar_arrive_relaxed_warp(&sh.dq_free[bf]);  // not behind the previous chunk's adds
       if (!dq_rows) continue;
-      float *acc = a.dq_acc + ((int64_t)h * rows_all + q0 + i0) * D + dl;
+      float *acc = a.dq_acc + ((int64_t)h * rows_all + q0 + i0) * D + dh * DO + dl;
       const int rows = min(BQ, lq - i0);
 #pragma unroll
       for (int e = 0; e < BQ; ++e)
@@ -611,7 +667,8 @@ __global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdArgs a, int64_t 
 
 template <typename T, int D>
 cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
-  constexpr int kSmem = BwdCfg<D>::kSmem;
+  using C = BwdCfg<D>;
+  constexpr int kSmem = C::kSmem, BQ = C::BQ;
   const FwdArgs &f = a.f;
   const int64_t rows_q = f.seqs.cu_q ? f.seqs.total_q : (int64_t)f.batch * f.seqs.sq;
   const int64_t rows_k = f.seqs.cu_k ? f.seqs.total_k : (int64_t)f.batch * f.seqs.sk;
@@ -630,11 +687,14 @@ cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
     cudaError_t e = set_smem_once<bwd_tc_kernel<T, D>>(kSmem);
     if (e != cudaSuccess) return e;
     const int n_blocks = (f.seqs.sk + BN - 1) / BN;
-    const int64_t grid = (int64_t)n_blocks * f.hkv * f.batch;
+    const int64_t grid = (int64_t)C::NH * n_blocks * f.hkv * f.batch;
     if (grid > INT32_MAX) return cudaErrorInvalidValue;
-    debug_log("backward: bwd_tc_kernel d=%d, %d keys per CTA, %d-query chunks, dQ %s, "
-              "grid=%lld CTAs x %d threads, smem=%d B", D, BN, BQ,
-              a.deterministic ? "by the query-stationary kernel (deterministic)" : "atomic fp32 adds",
+    debug_log("backward: bwd_tc_kernel d=%d, %d keys per CTA, %d output columns per CTA, "
+              "%d-query chunks, %d-stage ring, dQ %s, grid=%lld CTAs x %d threads, smem=%d B",
+              D, BN, C::DO, BQ, C::ST,
+              !a.deterministic ? "atomic fp32 adds"
+              : D == 256 ? "by the row kernel (deterministic)"
+                         : "by the query-stationary kernel (deterministic)",
               (long long)grid, kThreads, kSmem);
     bwd_tc_kernel<T, D><<<(unsigned)grid, kThreads, kSmem, st>>>(tq, tk, tv, tdo, a, n_blocks);
     count_launches(1);
@@ -645,8 +705,10 @@ cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   if (a.deterministic) {
-    // dQ from the query-stationary kernel: no atomics, the same bits every run
-    cudaError_t e = launch_bwd_dq_tc(a, st);
+    // dQ without atomics, the same bits every run: the query-stationary
+    // tensor-core kernel, or at d = 256 (whose 128 x 256 fp32 dQ tile does not
+    // fit next to S and dP in TMEM) the row kernel, one warp per query row
+    cudaError_t e = D == 256 ? launch_bwd_dq_rows(a, st) : launch_bwd_dq_tc(a, st);
     if (e != cudaSuccess) return e;
   } else if (rows_q > 0) {
     const int64_t n4 = rows_q * f.hq * D / 4;
@@ -664,6 +726,7 @@ cudaError_t launch_bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
   switch (a.f.d) {
     case 64: return bf ? bwd_tc<__nv_bfloat16, 64>(a, sms, st) : bwd_tc<__half, 64>(a, sms, st);
     case 128: return bf ? bwd_tc<__nv_bfloat16, 128>(a, sms, st) : bwd_tc<__half, 128>(a, sms, st);
+    case 256: return bf ? bwd_tc<__nv_bfloat16, 256>(a, sms, st) : bwd_tc<__half, 256>(a, sms, st);
   }
   return cudaErrorInvalidValue;
 }

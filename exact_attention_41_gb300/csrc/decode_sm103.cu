@@ -14,7 +14,7 @@
 // page (page_size % 128 == 0), fetched by TMA from the page pool at the
 // physical row the block table gives.  Roles:
 //
-//   warp 0     TMA producer (Q once, then K and V tiles, 2-stage ring)
+//   warp 0     TMA producer (Q once, then K and V tiles, 3-stage ring)
 //   warp 1     MMA issuer
 //   warps 2-5  one thread per key (TMEM lane): mask, column max across the
 //              CTA, exp, P into shared memory; the same threads own the d
@@ -34,7 +34,7 @@ using namespace sm103;
 
 constexpr int D = 128;
 constexpr int BK = 128;  // keys per tile
-constexpr int ST = 2;
+constexpr int ST = 3;
 constexpr int kThreads = 192;
 constexpr int kTile = BK * D * 2;  // 32 KB
 constexpr float kRescaleThreshold = 8.0f;
@@ -67,6 +67,13 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// Maximum of v over the 32 lanes of the warp (all lanes active).
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 
 __device__ __forceinline__ bool wait_bar(DecShared &sh, uint64_t *bar, uint32_t parity, int *err) {
@@ -338,12 +345,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         x[q] = vis ? (cap ? cap_out * tanh_fast(s * cap_in) : s * sl2) : -INFINITY;
         tmax[q] = x[q];
       }
-      // column max over the 128 keys of the tile: warp shuffle, then across warps
+      // column max over the 128 keys of the tile: one warp reduction per
+      // column, then across warps
 #pragma unroll
-      for (int q = 0; q < RP; ++q) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) tmax[q] = fmaxf(tmax[q], __shfl_xor_sync(0xffffffffu, tmax[q], o));
-      }
+      for (int q = 0; q < RP; ++q) tmax[q] = warp_max(tmax[q]);
       // lane q publishes column q; the buffer alternates per tile, so the
       // barrier of tile j also ends every read of tile j-1's buffer
       float mine = -INFINITY;

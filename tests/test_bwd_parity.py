@@ -88,12 +88,13 @@ def test_training_shape_sampled_groups(deterministic):
 @pytest.mark.parametrize("deterministic", [False, True])
 @pytest.mark.parametrize("dtype,d,hq,hkv,s", [(syn.BF16, 64, 8, 2, 1024), (syn.F16, 64, 8, 2, 777),
                                               (syn.F16, 128, 8, 2, 2048),
-                                              (syn.BF16, 256, 4, 2, 384)])
+                                              (syn.BF16, 256, 4, 2, 384),
+                                              (syn.F16, 256, 8, 2, 1000)])
 @pytest.mark.parametrize("kw", [dict(causal=True), dict(causal=True, window=(100, 0), softcap=8.0)])
 def test_larger_head_dims_and_fp16(deterministic, dtype, d, hq, hkv, s, kw):
-    """Beyond the small shapes: d = 64 (tensor cores, like d = 128), d = 256
-    (CUDA-core row kernels) and fp16 at d = 128, over several key blocks and
-    query chunks with a ragged tail (777 rows), both dQ modes.
+    """Beyond the small shapes: d = 64, d = 256 (32-query chunks, one CTA per
+    128-column half) and fp16 at d = 128, over several key blocks and query
+    chunks with a ragged tail (777 rows), both dQ modes.
 
     The backward is a function of (Q, K, V, O, LSE, dO): here O (rounded to
     the storage type) and LSE come from the oracle's forward, so both sides
