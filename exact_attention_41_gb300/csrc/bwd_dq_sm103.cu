@@ -388,6 +388,8 @@ cudaError_t bwd_dq(const BwdArgs &a, cudaStream_t st) {
       !make_map_3d(&tv, f.v, f.dtype, rows_k, f.hkv, D, BN, f.v_rs))
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem_once<bwd_dq_kernel<T, D>>(kSmem);
+  if (e == cudaSuccess)  // 128 * 88 + 256 * 208 after setmaxnreg
+    e = check_regs_once<bwd_dq_kernel<T, D>>(kThreads, 128 * 88 + 256 * 208);
   if (e != cudaSuccess) return e;
   const int m_blocks = (f.seqs.sq + BM - 1) / BM;
   const int64_t grid = (int64_t)m_blocks * f.hq * f.batch;

@@ -685,6 +685,8 @@ cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
         !make_map_3d(&tv, f.v, f.dtype, rows_k, f.hkv, D, BN, f.v_rs))
       return cudaErrorInvalidValue;
     cudaError_t e = set_smem_once<bwd_tc_kernel<T, D>>(kSmem);
+    if (e == cudaSuccess)  // 128 * (104 + 2 * 152 + 104) after setmaxnreg
+      e = check_regs_once<bwd_tc_kernel<T, D>>(kThreads, 128 * (104 + 2 * 152 + 104));
     if (e != cudaSuccess) return e;
     const int n_blocks = (f.seqs.sk + BN - 1) / BN;
     const int64_t grid = (int64_t)C::NH * n_blocks * f.hkv * f.batch;

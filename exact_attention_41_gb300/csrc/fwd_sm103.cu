@@ -597,6 +597,8 @@ cudaError_t fwd_tc(const FwdArgs &a, cudaStream_t st) {
       !make_map_3d(&tv, a.v, a.dtype, rows_k, a.hkv, D, BN, a.v_rs))
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem_once<fwd_tc_kernel<T, D, BN, NT, QB>>(C::kSmem);
+  if (e == cudaSuccess && NT == 2)  // 128 * 88 + 256 * 208 after setmaxnreg
+    e = check_regs_once<fwd_tc_kernel<T, D, BN, NT, QB>>(C::kThreads, 128 * 88 + 256 * 208);
   if (e != cudaSuccess) return e;
   const int block_pos = kBM / pg * NT;  // query positions per CTA
   const int m_blocks = (a.seqs.sq + block_pos - 1) / block_pos;

@@ -108,6 +108,29 @@ cudaError_t set_smem_once(int bytes) {
   return e;
 }
 
+// Kernels whose warpgroups move registers between them with setmaxnreg need
+// the CTA to be launched with at least `needed` registers in all (threads x
+// registers a thread, the latter as compiled, rounded up to 8): a split
+// above that would leave an increase waiting forever.  Checked once per
+// process from the compiled kernel; a kernel that fails it is not launched.
+template <auto Kernel>
+cudaError_t check_regs_once(int threads, int needed) {
+  static std::atomic<int> state{0};  // 0 unknown, 1 fits, 2 does not
+  int s = state.load(std::memory_order_acquire);
+  if (s == 0) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, Kernel);
+    if (e != cudaSuccess) return e;
+    const int regs = (fa.numRegs + 7) / 8 * 8;
+    s = regs * threads >= needed ? 1 : 2;
+    if (s == 2)
+      debug_log("register split of %d needs %d registers a CTA; compiled with %d a thread x %d",
+                needed, needed, fa.numRegs, threads);
+    state.store(s, std::memory_order_release);
+  }
+  return s == 1 ? cudaSuccess : cudaErrorInvalidConfiguration;
+}
+
 cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t st);
 cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t st);
 // dQ of the backward, query-stationary (d = 64, 128): written once, no atomics.
