@@ -120,6 +120,11 @@ def sources_sha(names):
     return h.hexdigest()[:16]
 
 
+TRAFFIC_NOTE = ("DRAM bytes seen during one launch (dram__bytes_read + dram__bytes_write, "
+                "ncu capture of the b=1 case scaled by 4); writes still held in L2 when the "
+                "kernel ends are not in it")
+
+
 def traffic_for(kernel_key):
     """DRAM bytes per launch from a committed ncu summary, if the kernel's
     sources are unchanged since that capture; else None."""
@@ -230,8 +235,7 @@ def bench_varlen(libattn, steps, stream):
 def bench_head_dims(libattn, steps, stream):
     """Forward and backward TFLOP/s at head dims 64 and 256 beside 128, on a
     causal bf16 problem of the training shape's kind (b=2, s=4096, GQA 4:1,
-    hq * d = 4096), both dQ modes.  Every backward runs on the tensor cores;
-    at d = 256 the deterministic dQ comes from the row kernel."""
+    hq * d = 4096), both dQ modes, all on the tensor cores."""
     import torch
 
     out = {}
@@ -257,7 +261,7 @@ def bench_head_dims(libattn, steps, stream):
         g()
         g(True)
         tf, tb = timed(f, steps, stream), timed(g, steps, stream)
-        td = timed(lambda: g(True), steps if d != 256 else 2, stream)
+        td = timed(lambda: g(True), steps, stream)
         out[f"d{d}"] = {"fwd_ms": round(tf, 4), "fwd_tflops": round(flops / tf / 1e9, 2),
                         "bwd_ms": round(tb, 4), "bwd_tflops": round(2.5 * flops / tb / 1e9, 2),
                         "bwd_deterministic_ms": round(td, 4),
@@ -645,12 +649,13 @@ def run_ours(args, rank, world, local_rank):
             "roofline": {"bound": "tensor", "kernel": "backward (attn_bwd call)",
                          "achieved": round(bwd_tflops, 2), "peak": peak_t, "unit": "TFLOP/s",
                          "frac": round(bwd_tflops / peak_t, 4),
-                         "traffic": traffic_for("bwd"),
+                         "traffic": traffic_for("bwd"), "traffic_note": TRAFFIC_NOTE,
                          "per_launch": "algorithmic bwd FLOPs 5.498e12 / CUDA-event time of "
                                        "one attn_bwd call"},
             "roofline_fwd": {"bound": "tensor", "kernel": "forward (attn_fwd call)",
                              "achieved": round(fwd_tflops, 2), "peak": peak_t, "unit": "TFLOP/s",
-                             "frac": round(fwd_tflops / peak_t, 4), "traffic": traffic_for("fwd")},
+                             "frac": round(fwd_tflops / peak_t, 4), "traffic": traffic_for("fwd"),
+                             "traffic_note": TRAFFIC_NOTE},
             "e2e": {"value": round(world * STEP_FLOPS / (ms_e2e * 1e-3) / 1e12, 2),
                     "unit": "TFLOP/s", "ms_per_step": round(ms_e2e, 4), **e2e_info},
             "gpu_launches": launches,
@@ -686,7 +691,8 @@ def run_profile_case(args):
     streams and about 1 GB on the device at most:
 
     fwd / bwd   causal bf16 b=1 s=8192 hq=32 hkv=8 d=128 (`--deterministic`
-                for that backward mode)
+                for that backward mode; `--head-dim` 64 or 256 keeps
+                hq * d = 4096 and hkv = hq / 4, as the head-dim sweep does)
     decode      paged decode b=16, sq=s_new=4 (--decode-sq), hq=32 hkv=8, caches U[1,32768]
                 in 256-token pages (the workload's per-entry shape; 16 entries
                 make several full waves of splits)
@@ -705,15 +711,17 @@ def run_profile_case(args):
 
     bf = syn.BF16
     if args.profile_case in ("fwd", "bwd"):
-        b, s, hq, hkv = 1, S, HQ, HKV
-        q = syn.device_normal((b, s, hq, D), bf, 1)
-        k = syn.device_normal((b, s, hkv, D), bf, 2)
-        v = syn.device_normal((b, s, hkv, D), bf, 3)
+        d = args.head_dim
+        b, s, hq = 1, S, HQ * D // d
+        hkv = hq // 4
+        q = syn.device_normal((b, s, hq, d), bf, 1)
+        k = syn.device_normal((b, s, hkv, d), bf, 2)
+        v = syn.device_normal((b, s, hkv, d), bf, 3)
         if args.profile_case == "fwd":
             for _ in range(args.calls):
                 libattn.fwd(q, k, v, causal=True)
         else:
-            do = syn.device_normal((b, s, hq, D), bf, 4)
+            do = syn.device_normal((b, s, hq, d), bf, 4)
             o, lse = libattn.fwd(q, k, v, causal=True)
             for _ in range(args.calls):
                 libattn.bwd(q, k, v, o, lse, do, causal=True, deterministic=args.deterministic)
@@ -761,6 +769,8 @@ def main():
     ap.add_argument("--calls", type=int, default=2, help="calls of --profile-case")
     ap.add_argument("--deterministic", action="store_true", help="--profile-case bwd mode")
     ap.add_argument("--decode-sq", type=int, default=4, help="--profile-case decode: sq = s_new")
+    ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128, 256],
+                    help="--profile-case fwd/bwd: head dim (hq = 4096 / d)")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -1,13 +1,11 @@
-// Warp-per-row kernels (CUDA cores, fp32 math).
+// Warp-per-row forward (CUDA cores, fp32 math).
 //
 // One warp owns one query row.  Lanes take 32 keys at a time for the dot
 // products, and 32 column slices of the head dimension for the
-// accumulations, exchanging the per-key scalars with warp shuffles.  The
-// forward is the online softmax of "FlashAttention完整说明" §二.1 with key
-// blocks of 32; the dQ kernel recomputes P from Q, K and the saved LSE
-// (§二.2).  Used where the tensor-core kernels do not apply: the forward of a
-// problem with no keys at all, and dQ of the deterministic backward at
-// d = 256, whose 128 x 256 fp32 dQ tile does not fit in TMEM beside S and dP.
+// accumulation, exchanging the per-key scalars with warp shuffles: the
+// online softmax of "FlashAttention完整说明" §二.1 with key blocks of 32.
+// Used only where the tensor-core forward does not apply: a problem with no
+// keys at all (every row empty: O = 0, LSE = -inf).
 #include "kernels.h"
 
 namespace attn {
@@ -81,66 +79,6 @@ __global__ void __launch_bounds__(kWarps * 32) fwd_rows_kernel(FwdArgs a) {
     a.lse[a.seqs.lse_index(b, h, q0, i)] = l > 0.f ? (m + log2f(l)) * kLn2 : -INFINITY;
 }
 
-// dQ_i = scale * sum_j dS_ij k_j, one warp per query row (no atomics).
-template <typename T, int D>
-__global__ void __launch_bounds__(kWarps * 32) bwd_dq_rows_kernel(BwdArgs a) {
-  constexpr int V = D / 32;
-  __shared__ float qs[kWarps][D];
-  __shared__ float gs[kWarps][D];
-  const FwdArgs &f = a.f;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int b = blockIdx.z, h = blockIdx.y;
-  const int i = blockIdx.x * kWarps + warp;
-  int q0, lq, k0, lk;
-  if (!f.seqs.get(b, q0, lq, k0, lk, f.err) || i >= lq) return;
-  const int kvh = h / (f.hq / f.hkv);
-  const int64_t krs = f.k_rs, vrs = f.v_rs;
-  const int64_t qoff = (int64_t)(q0 + i) * f.q_rs + (int64_t)h * D;      // q
-  const int64_t goff = ((int64_t)(q0 + i) * f.hq + h) * D;             // dO (contiguous)
-  const T *kb = static_cast<const T *>(f.k) + (int64_t)k0 * krs + (int64_t)kvh * D;
-  const T *vb = static_cast<const T *>(f.v) + (int64_t)k0 * vrs + (int64_t)kvh * D;
-  for (int c = lane; c < D; c += 32) {
-    qs[warp][c] = Elem<T>::to_f(static_cast<const T *>(f.q)[qoff + c]);
-    gs[warp][c] = Elem<T>::to_f(static_cast<const T *>(a.dout)[goff + c]);
-  }
-  __syncwarp();
-  const int64_t li = f.seqs.lse_index(b, h, q0, i);
-  const float lse2 = f.lse[li] * kLog2e, dsum = a.dsum[li];
-  int lo, hi;
-  key_range(i, lq, lk, f.win_l, f.win_r, lo, hi);
-  float acc[V];
-#pragma unroll
-  for (int u = 0; u < V; ++u) acc[u] = 0.f;
-  for (int j0 = lo; j0 <= hi; j0 += 32) {
-    const int j = j0 + lane;
-    float ds = 0.f;
-    if (j <= hi) {
-      const float s_raw = dot_row<T, D>(qs[warp], kb + (int64_t)j * krs) * f.scale;
-      float s = s_raw, dcap = 1.f;
-      if (f.softcap > 0.f) {
-        const float t = tanhf(s_raw / f.softcap);
-        s = f.softcap * t;
-        dcap = 1.f - t * t;
-      }
-      const float p = exp2f(s * kLog2e - lse2);
-      const float dp = dot_row<T, D>(gs[warp], vb + (int64_t)j * vrs);
-      ds = p * (dp - dsum) * dcap;
-    }
-    const int n = min(32, hi - j0 + 1);
-    for (int jj = 0; jj < n; ++jj) {
-      const float dj = __shfl_sync(0xffffffffu, ds, jj);
-      float kk[V];
-      load_vec<T, V>(kb + (int64_t)(j0 + jj) * krs + lane * V, kk);
-#pragma unroll
-      for (int u = 0; u < V; ++u) acc[u] = fmaf(dj, kk[u], acc[u]);
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < V; ++u) acc[u] *= f.scale;
-  store_vec<T, V>(static_cast<T *>(a.dq) + (int64_t)(q0 + i) * a.dq_rs + (int64_t)h * D + lane * V,
-                  acc);
-}
-
 template <typename T, int D>
 cudaError_t fwd_rows(const FwdArgs &a, cudaStream_t st) {
   dim3 grid((a.seqs.sq + kWarps - 1) / kWarps, a.hq, a.batch);
@@ -160,30 +98,6 @@ cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t st) {
     case 256: return bf ? fwd_rows<__nv_bfloat16, 256>(a, st) : fwd_rows<__half, 256>(a, st);
   }
   return cudaErrorInvalidValue;
-}
-
-cudaError_t launch_bwd_dq_rows(const BwdArgs &a, cudaStream_t st) {
-  const FwdArgs &f = a.f;
-  const bool bf = f.dtype == ATTN_BF16;
-  dim3 gq((f.seqs.sq + kWarps - 1) / kWarps, f.hq, f.batch);
-  switch (f.d) {
-    case 64:
-      if (bf) bwd_dq_rows_kernel<__nv_bfloat16, 64><<<gq, kWarps * 32, 0, st>>>(a);
-      else bwd_dq_rows_kernel<__half, 64><<<gq, kWarps * 32, 0, st>>>(a);
-      break;
-    case 128:
-      if (bf) bwd_dq_rows_kernel<__nv_bfloat16, 128><<<gq, kWarps * 32, 0, st>>>(a);
-      else bwd_dq_rows_kernel<__half, 128><<<gq, kWarps * 32, 0, st>>>(a);
-      break;
-    case 256:
-      if (bf) bwd_dq_rows_kernel<__nv_bfloat16, 256><<<gq, kWarps * 32, 0, st>>>(a);
-      else bwd_dq_rows_kernel<__half, 256><<<gq, kWarps * 32, 0, st>>>(a);
-      break;
-    default:
-      return cudaErrorInvalidValue;
-  }
-  count_launches(1);
-  return cudaGetLastError();
 }
 
 }  // namespace attn

@@ -1,4 +1,5 @@
-// dQ of the backward, query-stationary, on the tensor cores (sm_103a), d = 64 or 128.
+// dQ of the backward, query-stationary, on the tensor cores (sm_103a), d = 64,
+// 128 or 256.
 //
 // dQ_i = scale * sum_j dS_ij k_j with dS = P * (dP - D), P = exp(s - LSE),
 // dP = dO V^T ("FlashAttention完整说明" §二.2: S and P are recomputed from
@@ -23,6 +24,12 @@
 // dP(j+1) once both warpgroups have read dP(j); dQ(j) once dS(j) is written;
 // S(j+2) into the buffer dQ(j) reads, behind it in issue order.  So while the
 // softmax works on tile j the tensor pipe runs dQ(j-1), S(j+1) and dP(j+1).
+//
+// d = 256: Q and dO of the tile take 128 KB, so keys come in steps of 64
+// (K and V tiles of 32 KB; 2 K stages, 1 V stage) and each CTA produces one
+// 128-column half of dQ (two CTAs per query tile, each recomputing S and
+// dP).  TMEM: S buffers at [0,64) / [64,128), dP at [128,192), dQ at
+// [192,320).
 #include <cudaTypedefs.h>
 
 #include "kernels.h"
@@ -33,20 +40,26 @@ namespace {
 using namespace sm103;
 
 constexpr int BM = 128;  // query rows per CTA
-constexpr int BN = 128;  // keys per step
-constexpr int KST = 3;   // K ring stages
-constexpr int VST = 2;   // V ring stages
 constexpr int kThreads = 384;
-constexpr uint32_t kColS = 0, kColDP = 256, kColDQ = 384;
 
-// Shared-memory sizes for head dimension D (64 or 128).
+// Tile shape for head dimension D (64, 128 or 256).
 template <int D>
 struct DqCfg {
-  static constexpr int kTile = 128 * D * 2;  // one 128-row tile of Q, dO, K or V: 32 KB at 128
-  static constexpr int kSmemData = 2 * kTile + (KST + VST) * kTile;  // 224 KB at d = 128
+  static constexpr int BN = D == 256 ? 64 : 128;   // keys per step
+  static constexpr int KST = D == 256 ? 2 : 3;     // K ring stages
+  static constexpr int VST = D == 256 ? 1 : 2;     // V ring stages
+  static constexpr int DO = D < 128 ? D : 128;     // dQ columns of one CTA
+  static constexpr int NH = D / DO;                // CTAs per query tile
+  static constexpr uint32_t kColS = 0, kColDP = 2 * BN, kColDQ = 3 * BN;
+  static constexpr int kQTile = BM * D * 2;        // Q or dO of the tile: 32 KB at d = 128
+  static constexpr int kKTile = BN * D * 2;        // one K or V tile
+  static constexpr int kSmemData = 2 * kQTile + (KST + VST) * kKTile;  // 224 KB
   static constexpr int kSmem = kSmemData + 1024;
+  static_assert(kSmem <= 227 * 1024 - 1024, "shared memory");
+  static_assert(kColDQ + DO <= 512, "TMEM");
 };
 
+template <int KST, int VST>
 struct Shared {
   uint64_t q_full;
   uint64_t k_full[KST], k_empty[KST], v_full[VST], v_empty[VST];
@@ -66,11 +79,13 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-__device__ __forceinline__ bool wait_bar(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
+template <typename Sh>
+__device__ __forceinline__ bool wait_bar(Sh &sh, uint64_t *bar, uint32_t parity, int *err) {
   return mbar_wait_bounded(smem_u32(bar), parity, &sh.abort, err, sh.wait_ns);
 }
 
-__device__ __forceinline__ bool wait_warp(Shared &sh, uint64_t *bar, uint32_t parity, int *err) {
+template <typename Sh>
+__device__ __forceinline__ bool wait_warp(Sh &sh, uint64_t *bar, uint32_t parity, int *err) {
   return __all_sync(0xffffffffu, wait_bar(sh, bar, parity, err));
 }
 
@@ -82,20 +97,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                   const BwdArgs a, const int m_blocks) {
-  constexpr int kTile = DqCfg<D>::kTile;
+  using C = DqCfg<D>;
+  constexpr int BN = C::BN, KST = C::KST, VST = C::VST, DO = C::DO;
+  constexpr int kQTile = C::kQTile, kKTile = C::kKTile;
+  constexpr uint32_t kColS = C::kColS, kColDP = C::kColDP, kColDQ = C::kColDQ;
   const FwdArgs &f = a.f;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ Shared sh;
+  __shared__ Shared<KST, VST> sh;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   uint8_t *q_s = smem;
-  uint8_t *do_s = smem + kTile;
-  uint8_t *k_s = smem + 2 * kTile;        // [KST]
-  uint8_t *v_s = k_s + KST * kTile;       // [VST]
+  uint8_t *do_s = smem + kQTile;
+  uint8_t *k_s = smem + 2 * kQTile;       // [KST]
+  uint8_t *v_s = k_s + KST * kKTile;      // [VST]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // CTA -> (query block, batch, head): heaviest blocks first, heads fastest
-  const int bid = blockIdx.x;
+  // CTA -> (column half, query block, batch, head): heaviest blocks first,
+  // heads fastest; dh selects the dQ columns [dh DO, dh DO + DO)
+  const int dh = blockIdx.x % C::NH;
+  const int bid = blockIdx.x / C::NH;
   const int h = bid % f.hq;
   const int b = (bid / f.hq) % f.batch;
   const int mb = m_blocks - 1 - bid / (f.hq * f.batch);
@@ -153,7 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tk);
         prefetch_tmap(&tv);
         prefetch_tmap(&tdo);
-        mbar_expect_tx(&sh.q_full, 2 * kTile);
+        mbar_expect_tx(&sh.q_full, 2 * kQTile);
         for (int c = 0; c < D / 64; ++c) {
           tma_load_3d(q_s + c * BM * 128, &tq, &sh.q_full, c * 64, h, q0 + m0);
           tma_load_3d(do_s + c * BM * 128, &tdo, &sh.q_full, c * 64, h, q0 + m0);
@@ -163,14 +183,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int krow = k0 + (n_lo + j) * BN;
           const int ks = j % KST, vs = j % VST;
           if (!wait_bar(sh, &sh.k_empty[ks], ((j / KST) & 1) ^ 1, f.err)) break;
-          mbar_expect_tx(&sh.k_full[ks], kTile);
+          mbar_expect_tx(&sh.k_full[ks], kKTile);
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(k_s + ks * kTile + c * BN * 128, &tk, &sh.k_full[ks], c * 64, kvh, krow);
+            tma_load_3d(k_s + ks * kKTile + c * BN * 128, &tk, &sh.k_full[ks], c * 64, kvh, krow);
           k_issued = j + 1;
           if (!wait_bar(sh, &sh.v_empty[vs], ((j / VST) & 1) ^ 1, f.err)) break;
-          mbar_expect_tx(&sh.v_full[vs], kTile);
+          mbar_expect_tx(&sh.v_full[vs], kKTile);
           for (int c = 0; c < D / 64; ++c)
-            tma_load_3d(v_s + vs * kTile + c * BN * 128, &tv, &sh.v_full[vs], c * 64, kvh, krow);
+            tma_load_3d(v_s + vs * kKTile + c * BN * 128, &tv, &sh.v_full[vs], c * 64, kvh, krow);
           v_issued = j + 1;
         }
         if (*(volatile int *)&sh.abort) {
@@ -188,18 +208,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (elect_one() && nt > 0) {
         constexpr int ab = IsBf16<T>::v;
         constexpr uint32_t id_s = idesc_f16(BM, BN, ab, 0, 0);  // S, dP (K-major A and B)
-        constexpr uint32_t id_q = idesc_f16(BM, D, ab, 0, 1);   // dQ (A = dS in TMEM, B = K MN-major)
+        constexpr uint32_t id_q = idesc_f16(BM, DO, ab, 0, 1);  // dQ (A = dS in TMEM, B = K MN-major)
         const uint64_t q_d = smem_desc(smem_u32(q_s), 16, 1024);
         const uint64_t do_d = smem_desc(smem_u32(do_s), 16, 1024);
         const uint64_t k_d = smem_desc(smem_u32(k_s), 16, 1024);
         const uint64_t v_d = smem_desc(smem_u32(v_s), 16, 1024);
-        const uint64_t k_mn = smem_desc(smem_u32(k_s), BN * 128, 1024);
+        // K as dQ's B operand: this CTA's column half (64-column blocks 2 dh, 2 dh + 1)
+        const uint64_t k_mn = smem_desc(smem_u32(k_s) + dh * 2 * (BN * 128), BN * 128, 1024);
         // X (Q or dO) times the key tile's K or V rows, K = d
+        // (at d = 256 one 64-column block of d per outer step, not unrolled:
+        // 16 unrolled steps would keep too many descriptors live)
         auto mma_xk = [&](uint32_t dcol, uint64_t a_d, uint64_t b_d, uint32_t b_off) {
+          if constexpr (D == 256) {
+#pragma unroll 1
+            for (int cb = 0; cb < D / 64; ++cb) {
+              const uint64_t ab = desc_add(a_d, cb * (BM * 128));
+              const uint64_t bb = desc_add(b_d, b_off + cb * (BN * 128));
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t o = (kk / 4) * (128 * 128) + (kk % 4) * 32;
-            mma_ss(dcol, desc_add(a_d, o), desc_add(b_d, b_off + o), id_s, kk > 0);
+              for (int k4 = 0; k4 < 4; ++k4)
+                mma_ss(dcol, desc_add(ab, k4 * 32), desc_add(bb, k4 * 32), id_s, (cb | k4) > 0);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t oa = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+              const uint32_t ob = (kk / 4) * (BN * 128) + (kk % 4) * 32;
+              mma_ss(dcol, desc_add(a_d, oa), desc_add(b_d, b_off + ob), id_s, kk > 0);
+            }
           }
         };
         auto k_ready = [&](int j) {
@@ -213,11 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           return r;
         };
         auto issue_s = [&](int j) {  // S(j) = Q K_j^T into buffer j % 2
-          mma_xk(tmem + kColS + (j & 1) * 128, q_d, k_d, (j % KST) * kTile);
+          mma_xk(tmem + kColS + (j & 1) * BN, q_d, k_d, (j % KST) * kKTile);
           mma_commit(&sh.s_full[j & 1]);
         };
         auto issue_dp = [&](int j) {  // dP(j) = dO V_j^T
-          mma_xk(tmem + kColDP, do_d, v_d, (j % VST) * kTile);
+          mma_xk(tmem + kColDP, do_d, v_d, (j % VST) * kKTile);
           mma_commit(&sh.dp_full);
           mma_commit(&sh.v_empty[j % VST]);  // V_j is no longer read
         };
@@ -237,13 +272,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (!wait_bar(sh, &sh.ds_full[j & 1], (j >> 1) & 1, f.err)) break;
           tc_fence_after();
-          // dQ += dS(j) K_j: A = dS (keys 0-63 at the buffer's columns
-          // [0,32), keys 64-127 at [64,96)), B = K_j with d as N
-          const uint32_t sbuf = tmem + kColS + (j & 1) * 128;
-          const uint32_t ko = (j % KST) * kTile;
+          // dQ += dS(j) K_j: A = dS (warpgroup w's BN/2 keys packed at the
+          // buffer's columns BN/2 w + [0, BN/4)), B = K_j with d as N
+          const uint32_t sbuf = tmem + kColS + (j & 1) * BN;
+          const uint32_t ko = (j % KST) * kKTile;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(tmem + kColDQ, sbuf + (kk / 4) * 64 + (kk % 4) * 8,
+            mma_ts(tmem + kColDQ, sbuf + (BN / 2) * (16 * kk / (BN / 2)) + 8 * ((16 * kk % (BN / 2)) / 16),
                    desc_add(k_mn, ko + kk * 16 * 128), id_q, (j > 0 || kk > 0) ? 1u : 0u);
           mma_commit(&sh.k_empty[j % KST]);  // K_j is no longer read
           if (j + 2 < nt) {
@@ -283,26 +318,35 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t capx2 = f2_pack(cap_l2, cap_l2);
     bool ok = true;
     for (int j = 0; j < nt; ++j) {
-      const int key0 = (n_lo + j) * BN + 64 * w;  // first key of this warpgroup's half
+      const int key0 = (n_lo + j) * BN + (BN / 2) * w;  // first key of this warpgroup's half
       if (!wait_warp(sh, &sh.s_full[j & 1], (j >> 1) & 1, f.err) ||
           !wait_warp(sh, &sh.dp_full, j & 1, f.err)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t scol = lane_off + tmem + kColS + (j & 1) * 128 + 64 * w;
-      uint32_t su[64], du[64];
-      tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(su));
-      tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
-      tmem_ld32(lane_off + tmem + kColDP + 64 * w, *reinterpret_cast<uint32_t(*)[32]>(du));
-      tmem_ld32(lane_off + tmem + kColDP + 64 * w + 32, *reinterpret_cast<uint32_t(*)[32]>(du + 32));
+      constexpr int HK = BN / 2;  // keys of this warpgroup per step
+      const uint32_t scol = lane_off + tmem + kColS + (j & 1) * BN + HK * w;
+      const uint32_t dcol = lane_off + tmem + kColDP + HK * w;
+      uint32_t su[HK], du[HK];
+      // written out rather than as a loop over 32-column pieces: the loop
+      // form measured 15% slower at d = 128 (same registers, same spills)
+      if constexpr (HK == 64) {
+        tmem_ld32(scol, *reinterpret_cast<uint32_t(*)[32]>(su));
+        tmem_ld32(scol + 32, *reinterpret_cast<uint32_t(*)[32]>(su + 32));
+        tmem_ld32(dcol, *reinterpret_cast<uint32_t(*)[32]>(du));
+        tmem_ld32(dcol + 32, *reinterpret_cast<uint32_t(*)[32]>(du + 32));
+      } else {
+        tmem_ld32(scol, su);
+        tmem_ld32(dcol, du);
+      }
       tmem_wait_ld();
       tc_fence_before();
       mbar_arrive_warp(&sh.dp_free);  // dP(j+1) may overwrite the dP columns
-      const bool need_mask = !valid || key0 < lo_tile_max || key0 + 63 > hi_tile_min;
-      uint32_t pk[32];
+      const bool need_mask = !valid || key0 < lo_tile_max || key0 + HK - 1 > hi_tile_min;
+      uint32_t pk[HK / 2];
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
+      for (int q = 0; q < HK / 2; ++q) {
         const int c = 2 * q;
         const uint64_t s2 = f2_pack(__uint_as_float(su[c]), __uint_as_float(su[c + 1]));
         const uint64_t dp2 = f2_pack(__uint_as_float(du[c]), __uint_as_float(du[c + 1]));
@@ -332,20 +376,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       // dS (16-bit) over the first half of this warpgroup's S columns: the A
       // operand of dQ += dS K
       tmem_st16(scol, pk);
-      tmem_st16(scol + 16, pk + 16);
+      if constexpr (HK == 64) tmem_st16(scol + 16, pk + 16);
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive_warp(&sh.ds_full[j & 1]);
     }
-    // epilogue: dQ = scale * accumulated dS K; warpgroup w writes d columns
-    // [64 w, 64 w + 64)
+    // epilogue: dQ = scale * accumulated dS K; warpgroup w writes columns
+    // [DO/2 w, DO/2 w + DO/2) of this CTA's half
     if (ok && nt > 0) ok = wait_warp(sh, &sh.all_done, 0, f.err);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     if (ok) {
-      T *row = static_cast<T *>(a.dq) + (int64_t)(q0 + (valid ? i : 0)) * a.dq_rs + (int64_t)h * D;
+      T *row = static_cast<T *>(a.dq) + (int64_t)(q0 + (valid ? i : 0)) * a.dq_rs +
+               (int64_t)h * D + dh * DO;
 #pragma unroll 1
-      for (int c = w * (D / 64); c < (w + 1) * (D / 64); ++c) {
+      for (int c = w * (DO / 64); c < (w + 1) * (DO / 64); ++c) {
         uint32_t u[32];
         if (nt > 0) {
           tmem_ld32(lane_off + tmem + kColDQ + c * 32, u);
@@ -374,7 +419,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <typename T, int D>
 cudaError_t bwd_dq(const BwdArgs &a, cudaStream_t st) {
-  constexpr int kSmem = DqCfg<D>::kSmem;
+  using C = DqCfg<D>;
+  constexpr int kSmem = C::kSmem, BN = C::BN;
   const FwdArgs &f = a.f;
   const int64_t rows_q = f.seqs.cu_q ? f.seqs.total_q : (int64_t)f.batch * f.seqs.sq;
   const int64_t rows_k = f.seqs.cu_k ? f.seqs.total_k : (int64_t)f.batch * f.seqs.sk;
@@ -392,12 +438,12 @@ cudaError_t bwd_dq(const BwdArgs &a, cudaStream_t st) {
     e = check_regs_once<bwd_dq_kernel<T, D>>(kThreads, 128 * 88 + 256 * 208);
   if (e != cudaSuccess) return e;
   const int m_blocks = (f.seqs.sq + BM - 1) / BM;
-  const int64_t grid = (int64_t)m_blocks * f.hq * f.batch;
+  const int64_t grid = (int64_t)C::NH * m_blocks * f.hq * f.batch;
   if (grid == 0) return cudaSuccess;
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
-  debug_log("backward dQ (deterministic): bwd_dq_kernel d=%d, one %d-row query tile per CTA, "
-            "%d-key steps, grid=%lld CTAs x %d threads, smem=%d B", D, BM, BN, (long long)grid,
-            kThreads, kSmem);
+  debug_log("backward dQ (deterministic): bwd_dq_kernel d=%d, one %d-row query tile and %d dQ "
+            "columns per CTA, %d-key steps, grid=%lld CTAs x %d threads, smem=%d B", D, BM, C::DO,
+            BN, (long long)grid, kThreads, kSmem);
   bwd_dq_kernel<T, D><<<(unsigned)grid, kThreads, kSmem, st>>>(tq, tk, tv, tdo, a, m_blocks);
   count_launches(1);
   return cudaGetLastError();
@@ -410,6 +456,7 @@ cudaError_t launch_bwd_dq_tc(const BwdArgs &a, cudaStream_t st) {
   switch (a.f.d) {
     case 64: return bf ? bwd_dq<__nv_bfloat16, 64>(a, st) : bwd_dq<__half, 64>(a, st);
     case 128: return bf ? bwd_dq<__nv_bfloat16, 128>(a, st) : bwd_dq<__half, 128>(a, st);
+    case 256: return bf ? bwd_dq<__nv_bfloat16, 256>(a, st) : bwd_dq<__half, 256>(a, st);
   }
   return cudaErrorInvalidValue;
 }

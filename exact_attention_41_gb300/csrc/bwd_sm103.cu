@@ -694,9 +694,7 @@ cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
     debug_log("backward: bwd_tc_kernel d=%d, %d keys per CTA, %d output columns per CTA, "
               "%d-query chunks, %d-stage ring, dQ %s, grid=%lld CTAs x %d threads, smem=%d B",
               D, BN, C::DO, BQ, C::ST,
-              !a.deterministic ? "atomic fp32 adds"
-              : D == 256 ? "by the row kernel (deterministic)"
-                         : "by the query-stationary kernel (deterministic)",
+              a.deterministic ? "by the query-stationary kernel (deterministic)" : "atomic fp32 adds",
               (long long)grid, kThreads, kSmem);
     bwd_tc_kernel<T, D><<<(unsigned)grid, kThreads, kSmem, st>>>(tq, tk, tv, tdo, a, n_blocks);
     count_launches(1);
@@ -707,10 +705,8 @@ cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   if (a.deterministic) {
-    // dQ without atomics, the same bits every run: the query-stationary
-    // tensor-core kernel, or at d = 256 (whose 128 x 256 fp32 dQ tile does not
-    // fit next to S and dP in TMEM) the row kernel, one warp per query row
-    cudaError_t e = D == 256 ? launch_bwd_dq_rows(a, st) : launch_bwd_dq_tc(a, st);
+    // dQ from the query-stationary kernel: no atomics, the same bits every run
+    cudaError_t e = launch_bwd_dq_tc(a, st);
     if (e != cudaSuccess) return e;
   } else if (rows_q > 0) {
     const int64_t n4 = rows_q * f.hq * D / 4;

@@ -426,6 +426,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
     const uint32_t o_t = tmem + lane_off + t * D;
     int lo_i, hi_i;
     key_range(i, lq, lk, a.win_l, a.win_r, lo_i, hi_i);
+    const uint32_t n_vis = (uint32_t)max(hi_i - lo_i + 1, 0);  // keys this row sees
     // tiles that need no mask: every row of the tile sees every key in them
     int lo_tile_max, hi_tile_min, dummy;
     key_range(m0 + t * tile_pos + tile_pos - 1, lq, lk, a.win_l, a.win_r, lo_tile_max, dummy);
@@ -433,6 +434,7 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
     const float sl2 = a.scale * kLog2e;
     const bool cap = a.softcap > 0.f;
     const float cap_in = cap ? a.scale / a.softcap : 0.f, cap_out = a.softcap * kLog2e;
+    const float cap_k = cap_in * 2.8853900817779268f;  // 2 log2(e) cap_in
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     // this tile's own key tiles: n_lo + ta + j for j in [0, ntt)
@@ -458,16 +460,25 @@ __global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
       }
       // softcap, then the mask (Inference Cookbook FAQ Q22 order)
       if (cap) {
+        // c tanh(x cap_in) in log2 units = cap_out - 2 cap_out / (e^{2 x cap_in} + 1),
+        // two scores at a time (the exponential and the reciprocal on MUFU)
+        const uint64_t k2 = f2_pack(cap_k, cap_k), one2 = f2_pack(1.f, 1.f);
+        const uint64_t co2 = f2_pack(cap_out, cap_out), mco2 = f2_pack(-2.f * cap_out, -2.f * cap_out);
 #pragma unroll
-        for (int e = 0; e < BN; ++e) x[e] = cap_out * tanh_fast(x[e] * cap_in);
+        for (int e = 0; e < BN; e += 2) {
+          float a0, a1, y0, y1;
+          f2_unpack(f2_mul(f2_pack(x[e], x[e + 1]), k2), a0, a1);
+          f2_unpack(f2_add(f2_pack(ex2(a0), ex2(a1)), one2), y0, y1);
+          f2_unpack(f2_fma(f2_pack(rcp_approx(y0), rcp_approx(y1)), mco2, co2), x[e], x[e + 1]);
+        }
       }
       const bool need_mask = key0 < lo_tile_max || key0 + BN - 1 > hi_tile_min;
       if (need_mask) {
+        // visible: e - (lo_i - key0) in [0, n_vis), one unsigned compare per key
+        const int e_lo = lo_i - key0;
 #pragma unroll
-        for (int e = 0; e < BN; ++e) {
-          const int kj = key0 + e;
-          if (kj < lo_i || kj > hi_i) x[e] = -INFINITY;
-        }
+        for (int e = 0; e < BN; ++e)
+          if ((uint32_t)(e - e_lo) >= n_vis) x[e] = -INFINITY;
       }
       // raw-score max: scale and softcap preserve the order (scale >= 0);
       // eight independent partial maxima of three-input maxes keep the

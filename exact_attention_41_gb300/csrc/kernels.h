@@ -133,14 +133,11 @@ cudaError_t check_regs_once(int threads, int needed) {
 
 cudaError_t launch_fwd_simt(const FwdArgs &a, cudaStream_t st);
 cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t st);
-// dQ of the backward, query-stationary (d = 64, 128): written once, no atomics.
+// dQ of the backward, query-stationary (d = 64, 128, 256): written once, no atomics.
 cudaError_t launch_bwd_dq_tc(const BwdArgs &a, cudaStream_t st);
 // Backward on the tensor cores (d = 64, 128, 256): preprocess, key-stationary
 // dK/dV kernel (with atomic dQ unless deterministic), dQ finish.
 cudaError_t launch_bwd_tc(const BwdArgs &a, int sms, cudaStream_t st);
-// dQ alone by the row kernel (one warp per query row, no atomics); needs
-// dsum (D_i in the LSE layout) already computed.
-cudaError_t launch_bwd_dq_rows(const BwdArgs &a, cudaStream_t st);
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t st);
 // E4M3 -> bf16 widening of n (a multiple of 16) contiguous values.
 cudaError_t launch_widen_e4m3(const void *src, void *dst, int64_t n, int sms, cudaStream_t st);

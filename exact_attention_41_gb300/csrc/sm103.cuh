@@ -322,6 +322,13 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Hardware reciprocal (MUFU, relative error about 2^-22).
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
 // tanh(x) = 1 - 2 / (exp(2x) + 1), from the definition of tanh, with the
 // hardware 2^x and reciprocal (ex2.approx / rcp.approx: relative errors
 // around 2^-22): two MUFU operations instead of a library call.  The result
