@@ -59,8 +59,8 @@ struct DecShared {
   uint64_t wait_ns;   // wall-clock limit of a wait
   uint32_t tmem_base;
   int abort;
-  float wmax[2][4][32];
-  float wsum[4][32];
+  alignas(16) float wmax[2][4][32];
+  alignas(16) float wsum[4][32];
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -322,6 +322,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       qlo[q] = max(qlo[q], k_begin);
       qhi[q] = min(qhi[q], k_end - 1);
     }
+    // tiles inside [qlo_max, qhi_min] are seen whole by every live row
+    int qlo_max = k_begin, qhi_min = k_end - 1;
+#pragma unroll
+    for (int q = 0; q < RP; ++q) {
+      if (q < R) {
+        qlo_max = max(qlo_max, qlo[q]);
+        qhi_min = min(qhi_min, qhi[q]);
+      }
+    }
     float m_run[RP], l_part[RP];
 #pragma unroll
     for (int q = 0; q < RP; ++q) {
@@ -338,32 +347,61 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_wait_ld();
       float x[RP];
       float tmax[RP];
+      const int t0 = key - jl;
+      if (RP <= 16 && !cap && t0 >= qlo_max && t0 + BK - 1 <= qhi_min) {
+        // every live row sees the whole tile: no mask (the padding columns
+        // past R get scores of their zero rows, which touch only their own
+        // O^T columns and are never stored)
+        const uint64_t sl2x2 = f2_pack(sl2, sl2);
 #pragma unroll
-      for (int q = 0; q < RP; ++q) {
-        const float s = __uint_as_float(su[q]);
-        const bool vis = key >= qlo[q] && key <= qhi[q];
-        x[q] = vis ? (cap ? cap_out * tanh_fast(s * cap_in) : s * sl2) : -INFINITY;
-        tmax[q] = x[q];
+        for (int q = 0; q < RP; q += 2)
+          f2_unpack(f2_mul(f2_pack(__uint_as_float(su[q]), __uint_as_float(su[q + 1])), sl2x2),
+                    x[q], x[q + 1]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < RP; ++q) {
+          const float s = __uint_as_float(su[q]);
+          const bool vis = key >= qlo[q] && key <= qhi[q];
+          x[q] = vis ? (cap ? cap_out * tanh_fast(s * cap_in) : s * sl2) : -INFINITY;
+        }
       }
+#pragma unroll
+      for (int q = 0; q < RP; ++q) tmax[q] = x[q];
       // column max over the 128 keys of the tile: one warp reduction per
       // column, then across warps
 #pragma unroll
       for (int q = 0; q < RP; ++q) tmax[q] = warp_max(tmax[q]);
-      // lane q publishes column q; the buffer alternates per tile, so the
-      // barrier of tile j also ends every read of tile j-1's buffer
-      float mine = -INFINITY;
-#pragma unroll
-      for (int q = 0; q < RP; ++q)
-        if (lane == q) mine = tmax[q];
+      // lane 0 publishes the warp's column maxima (every lane holds them);
+      // the buffer alternates per tile, so the barrier of tile j also ends
+      // every read of tile j-1's buffer
       float(*wm)[32] = sh.wmax[j & 1];
-      if (lane < RP) wm[w4][lane] = mine;
+      if (lane == 0) {
+#pragma unroll
+        for (int q = 0; q < RP; q += 4)
+          *reinterpret_cast<float4 *>(&wm[w4][q]) = make_float4(tmax[q], tmax[q + 1], tmax[q + 2], tmax[q + 3]);
+      }
       mbar_arrive(&sh.grp);
       if (!wait_warp(sh, &sh.grp, j & 1, a.err)) { ok = false; break; }
       float alpha[RP];
       bool any_rescale = false;
+      float tms[RP];
+      if constexpr (RP <= 16) {
+#pragma unroll
+        for (int q = 0; q < RP; q += 4) {
+          const float4 w0 = *reinterpret_cast<const float4 *>(&wm[0][q]);
+          const float4 w1 = *reinterpret_cast<const float4 *>(&wm[1][q]);
+          const float4 w2 = *reinterpret_cast<const float4 *>(&wm[2][q]);
+          const float4 w3 = *reinterpret_cast<const float4 *>(&wm[3][q]);
+          tms[q] = fmaxf(fmax3(w0.x, w1.x, w2.x), w3.x);
+          tms[q + 1] = fmaxf(fmax3(w0.y, w1.y, w2.y), w3.y);
+          tms[q + 2] = fmaxf(fmax3(w0.z, w1.z, w2.z), w3.z);
+          tms[q + 3] = fmaxf(fmax3(w0.w, w1.w, w2.w), w3.w);
+        }
+      }
 #pragma unroll
       for (int q = 0; q < RP; ++q) {
-        const float tm = fmaxf(fmaxf(wm[0][q], wm[1][q]), fmaxf(wm[2][q], wm[3][q]));
+        // (32 columns: read one at a time, to stay within the registers)
+        const float tm = RP <= 16 ? tms[q] : fmaxf(fmax3(wm[0][q], wm[1][q], wm[2][q]), wm[3][q]);
         const float m_new = fmaxf(m_run[q], tm);
         alpha[q] = 1.f;
         if (m_new > m_run[q] + kRescaleThreshold) {
