@@ -174,6 +174,9 @@ __device__ __forceinline__ void p_ds_16(const uint32_t *su, const uint32_t *du, 
                                         float sl2, float cap_in, float cap_l2, uint32_t *ph,
                                         uint32_t *pl, uint32_t *dh, uint32_t *dl) {
   const uint64_t sl2x2 = f2_pack(sl2, sl2), cap_l2x2 = f2_pack(cap_l2, cap_l2);
+  const float capk = cap_in * 2.8853900817779268f;  // 2 log2(e) / c, times scale
+  const uint64_t capk2 = f2_pack(capk, capk), one2 = f2_pack(1.f, 1.f), mone2 = f2_pack(-1.f, -1.f);
+  const uint64_t two2 = f2_pack(2.f, 2.f), mtwo2 = f2_pack(-2.f, -2.f);
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     const int c = 2 * q;
@@ -184,11 +187,16 @@ __device__ __forceinline__ void p_ds_16(const uint32_t *su, const uint32_t *du, 
     float t0, t1;
     uint64_t dcap = 0;
     if constexpr (kCap) {
-      // capped score c tanh(s / c); its derivative factor is 1 - tanh^2
-      const float h0 = tanh_fast(__uint_as_float(su[c]) * cap_in);
-      const float h1 = tanh_fast(__uint_as_float(su[c + 1]) * cap_in);
-      f2_unpack(f2_fma(cap_l2x2, f2_pack(h0, h1), nl), t0, t1);
-      dcap = f2_pack(fmaf(-h0, h0, 1.f), fmaf(-h1, h1, 1.f));
+      // capped score c tanh(s / c), two at a time: tanh(u) = 1 - 2 r with
+      // r = 1 / (e^{2u} + 1) (MUFU exponential and reciprocal); its
+      // derivative factor is 1 - tanh^2
+      float a0, a1, y0, y1;
+      f2_unpack(f2_mul(s2, capk2), a0, a1);  // 2 u log2(e)
+      f2_unpack(f2_add(f2_pack(ex2(a0), ex2(a1)), one2), y0, y1);
+      const uint64_t r2 = f2_pack(rcp_approx(y0), rcp_approx(y1));
+      const uint64_t h2 = f2_fma(r2, mtwo2, one2), nh2 = f2_fma(r2, two2, mone2);
+      f2_unpack(f2_fma(cap_l2x2, h2, nl), t0, t1);
+      dcap = f2_fma(nh2, h2, one2);
     } else {
       f2_unpack(f2_fma(s2, sl2x2, nl), t0, t1);
     }

@@ -78,3 +78,40 @@ def test_workload_sampled_sequences(deterministic):
     assert_close(host(dq)[rows], rq[rows], syn.BF16, "dq")
     assert_close(host(dk)[rows], rk[rows], syn.BF16, "dk")
     assert_close(host(dv)[rows], rv[rows], syn.BF16, "dv")
+
+
+@pytest.mark.parametrize("deterministic", [False, True])
+@pytest.mark.parametrize("d", [64, 256])
+@pytest.mark.parametrize("kw", [dict(causal=True), dict(causal=True, window=(200, 0), softcap=30.0)])
+def test_packed_head_dims(deterministic, d, kw):
+    """Packed sequences at d = 64 and 256 (the backward's 64-column and
+    column-half layouts; ragged lengths, an empty-key sequence, sq != sk).
+    The forward is checked against the oracle; the backward is given the
+    oracle's O (rounded to bf16) and LSE, so it is checked as a function of
+    its inputs."""
+    import torch
+
+    from exact_attention_41_gb300 import libattn
+
+    lq = [300, 1, 129, 64, 200]
+    lk = [300, 7, 129, 0, 450]
+    dtype = syn.BF16
+    case = syn.varlen_case(33, lq, lk, 4, 2, d, dtype, with_dout=True)
+    o, lse, _ = run(case, lq, lk, dtype, with_bwd=False, **kw)
+    win = kw.get("window", (-1, -1))
+    args = [f64(case[x], dtype) for x in ("q", "k", "v")]
+    a = (case["cu_seqlens_q"], case["cu_seqlens_k"], 1 / math.sqrt(d), True,
+         win[0], win[1], kw.get("softcap", 0.0))
+    ro, rl = ref.varlen_forward(*args, *a)
+    assert_close(host(o), ro, dtype, "out")
+    assert_lse(host(lse), rl)
+    q, k, v, do = (dev(case[x], dtype) for x in ("q", "k", "v", "dout"))
+    cq, ck = dev_i32(case["cu_seqlens_q"]), dev_i32(case["cu_seqlens_k"])
+    o_ref = torch.from_numpy(ref.round_to(ro, dtype)).to(torch.bfloat16).cuda()
+    lse_ref = torch.from_numpy(rl.astype(np.float32)).cuda()
+    dq, dk, dv = libattn.bwd_varlen(q, k, v, o_ref, lse_ref, do, cq, ck, max(lq), max(lk),
+                                    deterministic=deterministic, **kw)
+    rq, rk, rv = ref.varlen_backward(*args, f64(case["dout"], dtype), *a, stored_o=dtype)
+    assert_close(host(dq), rq, dtype, "dq")
+    assert_close(host(dk), rk, dtype, "dk")
+    assert_close(host(dv), rv, dtype, "dv")
