@@ -77,7 +77,9 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when max gro
 // warpgroup per tile, TMEM = [O_0 | O_1 | S_0 | S_1]; the MMA warp alternates
 // between the tiles so one tile's softmax overlaps the other tile's MMAs, and
 // every K/V tile staged in shared memory serves 256 query rows.  NT = 1
-// (d = 256): TMEM = [O | S_a | S_b], S double-buffered instead.
+// (d = 256, and d = 128 under a window of at most 512 keys): TMEM = [O | S_a
+// | S_b], S double-buffered instead; at d = 128 with 64-key steps that is 256
+// TMEM columns and ~97 KB of shared memory, so two CTAs share an SM.
 // QB: bytes per Q/K element (2, or 1 for the E4M3 forward, whose V is bf16).
 template <int D, int BN, int NT, int QB = 2>
 struct FwdCfg {
@@ -87,15 +89,23 @@ struct FwdCfg {
   static constexpr int kKVBytes = BN * D * 2;   // one stage slot (V is 16-bit)
   static constexpr int kQKCols = D * QB / 128;  // 128-byte column blocks of Q / K
   static constexpr int kSmemData = NT * kQBytes + 2 * kStages * kKVBytes;
-  // at least ~120 KB so that one CTA owns the SM (and all 512 TMEM columns)
-  static constexpr int kSmem = (kSmemData + 1024 > 120 * 1024 ? kSmemData + 1024 : 120 * 1024);
+  // CTAs per SM: one tile with 64-key steps at d <= 128 fits two CTAs (TMEM
+  // O + 2 S = 256 columns, ~97 KB of shared memory), so one CTA's set-up,
+  // pipeline fill and epilogue overlap the other's work -- the short key
+  // ranges of a sliding window gain from that.  Otherwise one CTA owns the
+  // SM: at least ~120 KB of shared memory, all 512 TMEM columns.
+  static constexpr int kCtas = (NT == 1 && D <= 128) ? 2 : 1;
+  static constexpr int kSmem =
+      kCtas == 2 ? kSmemData + 1024
+                 : (kSmemData + 1024 > 120 * 1024 ? kSmemData + 1024 : 120 * 1024);
   static constexpr int kSCol0 = NT * D;
-  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmemCols = kCtas == 2 ? 256 : 512;
   // NT = 2: warpgroup 0 = producer, MMA and two idle warps; warpgroups 1-2 =
   // softmax.  NT = 1: warps 0-1 = producer, MMA; warps 2-5 = softmax.
   static constexpr int kThreads = NT == 2 ? 384 : 192;
   static constexpr int kSoftmaxWarp0 = NT == 2 ? 4 : 2;
-  static_assert(NT * D + 2 * BN <= 512, "TMEM budget");
+  static_assert(NT * D + 2 * BN <= (int)kTmemCols, "TMEM budget");
+  static_assert(kCtas == 1 || 2 * kSmem <= 227 * 1024, "shared memory of two CTAs");
 };
 
 struct Shared {
@@ -132,7 +142,7 @@ template <typename T>
 __device__ __forceinline__ uint32_t pack2(float a, float b) { return Elem<T>::from_f2(a, b); }
 
 template <typename T, int D, int BN, int NT, int QB>
-__global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, 1)
+__global__ void __launch_bounds__(FwdCfg<D, BN, NT, QB>::kThreads, FwdCfg<D, BN, NT, QB>::kCtas)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const FwdArgs a, const int m_blocks) {
   using C = FwdCfg<D, BN, NT, QB>;
@@ -634,6 +644,10 @@ cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t st) {
     case 64: return bf ? fwd_tc<__nv_bfloat16, 64, 128, 2>(a, st) : fwd_tc<__half, 64, 128, 2>(a, st);
     case 128:
       if (a.qk_fp8) return bf ? fwd_tc<__nv_bfloat16, 128, 128, 2, 1>(a, st) : cudaErrorInvalidValue;
+      // a window of at most 512 keys (besides the tile itself): short key
+      // ranges, one 128-row tile per CTA and two CTAs per SM
+      if (a.win_l >= 0 && a.win_r >= 0 && a.win_l + a.win_r <= 512)
+        return bf ? fwd_tc<__nv_bfloat16, 128, 64, 1>(a, st) : fwd_tc<__half, 128, 64, 1>(a, st);
       return bf ? fwd_tc<__nv_bfloat16, 128, 128, 2>(a, st) : fwd_tc<__half, 128, 128, 2>(a, st);
     case 256: return bf ? fwd_tc<__nv_bfloat16, 256, 64, 1>(a, st) : fwd_tc<__half, 256, 64, 1>(a, st);
   }
