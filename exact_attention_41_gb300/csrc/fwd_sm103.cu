@@ -77,7 +77,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O when max gro
 // warpgroup per tile, TMEM = [O_0 | O_1 | S_0 | S_1]; the MMA warp alternates
 // between the tiles so one tile's softmax overlaps the other tile's MMAs, and
 // every K/V tile staged in shared memory serves 256 query rows.  NT = 1
-// (d = 256, and d = 128 over at most 512 keys): TMEM = [O | S_a
+// (d = 256, and d = 128 over at most 1024 keys): TMEM = [O | S_a
 // | S_b], S double-buffered instead; at d = 128 with 64-key steps that is 256
 // TMEM columns and ~97 KB of shared memory, so two CTAs share an SM.
 // QB: bytes per Q/K element (2, or 1 for the E4M3 forward, whose V is bf16).
@@ -644,10 +644,10 @@ cudaError_t launch_fwd_tc(const FwdArgs &a, cudaStream_t st) {
     case 64: return bf ? fwd_tc<__nv_bfloat16, 64, 128, 2>(a, st) : fwd_tc<__half, 64, 128, 2>(a, st);
     case 128:
       if (a.qk_fp8) return bf ? fwd_tc<__nv_bfloat16, 128, 128, 2, 1>(a, st) : cudaErrorInvalidValue;
-      // a window of at most 512 keys (besides the tile itself) or sequences
-      // of at most 512 keys: short key ranges, one 128-row tile per CTA and
+      // a window of at most 1024 keys (besides the tile itself) or sequences
+      // of at most 1024 keys: short key ranges, one 128-row tile per CTA and
       // two CTAs per SM
-      if ((a.win_l >= 0 && a.win_r >= 0 && a.win_l + a.win_r <= 512) || a.seqs.sk <= 512)
+      if ((a.win_l >= 0 && a.win_r >= 0 && a.win_l + a.win_r <= 1024) || a.seqs.sk <= 1024)
         return bf ? fwd_tc<__nv_bfloat16, 128, 64, 1>(a, st) : fwd_tc<__half, 128, 64, 1>(a, st);
       return bf ? fwd_tc<__nv_bfloat16, 128, 128, 2>(a, st) : fwd_tc<__half, 128, 128, 2>(a, st);
     case 256: return bf ? fwd_tc<__nv_bfloat16, 256, 64, 1>(a, st) : fwd_tc<__half, 256, 64, 1>(a, st);
