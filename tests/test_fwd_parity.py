@@ -60,11 +60,26 @@ def test_bottom_right_causal_fp16(sq, sk, h, d):
     dict(softcap=2.5, window=(64, 64)),
 ])
 @pytest.mark.parametrize("shape", [(2, 197, 197, 8, 2, 128), (1, 300, 77, 4, 4, 64),
-                                   (1, 77, 300, 6, 3, 256), (3, 1, 513, 4, 1, 128)])
+                                   (1, 77, 300, 6, 3, 256), (3, 1, 513, 4, 1, 128),
+                                   (1, 1100, 1300, 4, 2, 128)])
 def test_masks_softcap_gqa_ragged(dtype, kw, shape):
+    """d = 128 takes two layouts: one 128-row tile with 64-key steps (two
+    CTAs per SM) for windows and sequences of at most 1024 keys, two tiles
+    with 128-key steps otherwise; the 1300-key shape keeps the unwindowed
+    cases on the second."""
     b, sq, sk, hq, hkv, d = shape
     o, lse, ro, rl = run_dense(11, b, sq, sk, hq, hkv, d, dtype, **kw)
     assert_close(o, ro, dtype, "out")
+    assert_lse(lse, rl)
+
+
+@pytest.mark.parametrize("kw", [dict(causal=True, window=(1100, 0), softcap=20.0),
+                                dict(window=(700, 700))])
+def test_wide_window_two_tile_layout(kw):
+    """Windows wider than 1024 keys at d = 128 run on the two-tile layout:
+    its masked tiles at both window edges, with and without softcap."""
+    o, lse, ro, rl = run_dense(13, 1, 2000, 2000, 4, 2, 128, syn.BF16, **kw)
+    assert_close(o, ro, syn.BF16, "out")
     assert_lse(lse, rl)
 
 
