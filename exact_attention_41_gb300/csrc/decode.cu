@@ -208,7 +208,7 @@ cudaError_t decode(const DecodeArgs &a, cudaStream_t st) {
     append_kernel<T><<<dim3(a.s_new, a.b), 128, 0, st>>>(a);
   }
   count_launches(a.s_new > 0);
-  // tensor-core kernel (d = 128, g * sq <= 32); warp-per-row kernel otherwise
+  // tensor-core kernel (g * sq <= 32, pages of 128-token multiples); warp-per-row kernel otherwise
   cudaError_t e = launch_decode_tc(a, st);
   if (e == cudaErrorNotSupported) {
     debug_log("decode: decode_rows_kernel (CUDA cores, one warp per query row) d=%d, "

@@ -1,4 +1,5 @@
-// Split-KV paged decode on the 5th-generation tensor cores (sm_103a), d = 128.
+// Split-KV paged decode on the 5th-generation tensor cores (sm_103a), d = 64,
+// 128 or 256.
 //
 // Inference Cookbook FAQ Q14/Q17/Q18.  One CTA owns one key range (split) of
 // one (batch entry, KV head) and all R = g * sq query rows that read that KV
@@ -22,6 +23,12 @@
 //
 // The output is the split's normalised partial O and its LSE (or the final
 // output when there is one split); decode.cu merges the splits.
+//
+// Head dims: at d = 64 the O^T product keeps M = 128 (its rows 64-127 read
+// the 16 KB after the V tile, padding included in the shared memory, and are
+// never stored); at d = 256 O^T is two M = 128 products, one per half of d,
+// and the 64 KB K and V tiles come through a 2-stage K ring and a 1-stage V
+// ring.
 #include <cudaTypedefs.h>
 
 #include "kernels.h"
@@ -32,27 +39,32 @@ namespace attn {
 namespace {
 using namespace sm103;
 
-constexpr int D = 128;
 constexpr int BK = 128;  // keys per tile
-constexpr int ST = 3;
 constexpr int kThreads = 192;
-constexpr int kTile = BK * D * 2;  // 32 KB
 constexpr float kRescaleThreshold = 8.0f;
 
-template <int RP>
+// Shapes for head dim D and RP (query rows padded to 16 or 32).
+template <int D, int RP>
 struct DecCfg {
+  static constexpr int KST = D == 256 ? 2 : 3;       // K ring stages
+  static constexpr int VST = D == 256 ? 1 : 3;       // V ring stages
+  static constexpr int kTile = BK * D * 2;           // one K or V tile: 32 KB at d = 128
   static constexpr int kQBytes = RP * D * 2;
   static constexpr int kPBytes = RP * BK * 2;
-  static constexpr int kSmemData = kQBytes + 2 * ST * kTile + 2 * kPBytes;
+  static constexpr int kPad = D == 64 ? kTile : 0;   // read past the last V tile by O^T's rows 64-127
+  static constexpr int kSmemData = kQBytes + (KST + VST) * kTile + 2 * kPBytes + kPad;
   static constexpr int kSmem = kSmemData + 1024;
-  static constexpr uint32_t kColS = 0;        // two S^T buffers of RP columns
-  static constexpr uint32_t kColO = 2 * RP;   // O^T
-  static constexpr uint32_t kTmemCols = RP == 16 ? 64 : 128;
+  static constexpr int kOHalves = D == 256 ? 2 : 1;  // O^T products of 128 rows
+  static constexpr uint32_t kColS = 0;               // two S^T buffers of RP columns
+  static constexpr uint32_t kColO = 2 * RP;          // O^T: kOHalves blocks of RP columns
+  static constexpr uint32_t kTmemCols = (2 + kOHalves) * RP <= 64 ? 64 : 128;
+  static_assert(kSmem + 2048 <= 227 * 1024, "shared memory");
 };
 
+template <int KST, int VST>
 struct DecShared {
   uint64_t q_full;
-  uint64_t k_full[ST], k_empty[ST], v_full[ST], v_empty[ST];
+  uint64_t k_full[KST], k_empty[KST], v_full[VST], v_empty[VST];
   uint64_t s_full[2], p_full[2], o_done;
   uint64_t grp;  // bounded barrier of the 128 softmax threads (one phase per use)
   uint64_t all_done;  // every MMA of the CTA has completed
@@ -76,7 +88,8 @@ __device__ __forceinline__ float warp_max(float v) {
   return r;
 }
 
-__device__ __forceinline__ bool wait_bar(DecShared &sh, uint64_t *bar, uint32_t parity, int *err) {
+template <typename Sh>
+__device__ __forceinline__ bool wait_bar(Sh &sh, uint64_t *bar, uint32_t parity, int *err) {
   return mbar_wait_bounded(smem_u32(bar), parity, &sh.abort, err, sh.wait_ns);
 }
 
@@ -85,7 +98,7 @@ __device__ __forceinline__ bool wait_bar(DecShared &sh, uint64_t *bar, uint32_t 
 // empty key set gives, so the combine step gives the split no weight and no
 // stale scratch value reaches the output.  The device error word records
 // the cause.  Thread `tid` of `nthreads` writes its share of the R rows.
-template <typename T>
+template <typename T, int D>
 __device__ __forceinline__ void store_empty_split(const DecodeArgs &a, int split, int bi, int kvh,
                                                   int R, int tid, int nthreads) {
   const int g = a.hq / a.hkv;
@@ -104,7 +117,8 @@ __device__ __forceinline__ void store_empty_split(const DecodeArgs &a, int split
 
 // The same wait taken by a whole warp with one answer, so warp-collective
 // tcgen05 loads/stores that follow are never reached by part of a warp.
-__device__ __forceinline__ bool wait_warp(DecShared &sh, uint64_t *bar, uint32_t parity, int *err) {
+template <typename Sh>
+__device__ __forceinline__ bool wait_warp(Sh &sh, uint64_t *bar, uint32_t parity, int *err) {
   return __all_sync(0xffffffffu, wait_bar(sh, bar, parity, err));
 }
 
@@ -139,19 +153,20 @@ __device__ __forceinline__ void tmem_st_rp(uint32_t taddr, uint32_t (&r)[RP]) {
   }
 }
 
-template <typename T, int RP>
+template <typename T, int D, int RP>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const DecodeArgs a) {
-  using C = DecCfg<RP>;
+  using C = DecCfg<D, RP>;
+  constexpr int KST = C::KST, VST = C::VST, kTile = C::kTile;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ DecShared sh;
+  __shared__ DecShared<KST, VST> sh;
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                               ~uintptr_t(1023));
   uint8_t *q_s = smem;
   uint8_t *k_s = smem + C::kQBytes;
-  uint8_t *v_s = k_s + ST * kTile;
-  uint8_t *p_s = v_s + ST * kTile;
+  uint8_t *v_s = k_s + KST * kTile;
+  uint8_t *p_s = v_s + VST * kTile;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = a.hq / a.hkv;
@@ -163,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int L = a.cache_seqlens[bi] + a.s_new;
   if (L < 0 || L > a.max_pages * a.page_size) {
     if (threadIdx.x == 0) raise_error(a.err, L < 0 ? kErrBadSeqlen : kErrCacheOverflow);
-    store_empty_split<T>(a, split, bi, kvh, R, threadIdx.x, kThreads);
+    store_empty_split<T, D>(a, split, bi, kvh, R, threadIdx.x, kThreads);
     return;
   }
   // keys any query row may see, clipped to this split
@@ -179,9 +194,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(&sh.q_full, 1);
-    for (int s = 0; s < ST; ++s) {
+    for (int s = 0; s < KST; ++s) {
       mbar_init(&sh.k_full[s], 1);
       mbar_init(&sh.k_empty[s], 1);
+    }
+    for (int s = 0; s < VST; ++s) {
       mbar_init(&sh.v_full[s], 1);
       mbar_init(&sh.v_empty[s], 1);
     }
@@ -200,9 +217,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(&sh.tmem_base, C::kTmemCols);
     tmem_relinquish();
   }
-  // rows R..RP-1 of the Q tile are padding: zero them once (both 64-column blocks)
-  for (int x = threadIdx.x; x < (RP - R) * 16; x += kThreads) {
-    const int row = R + x / 16, chunk = x % 16;
+  // rows R..RP-1 of the Q tile are padding: zero them once (all D/64
+  // column blocks, D/8 16-byte chunks a row)
+  for (int x = threadIdx.x; x < (RP - R) * (D / 8); x += kThreads) {
+    const int row = R + x / (D / 8), chunk = x % (D / 8);
     *reinterpret_cast<uint4 *>(q_s + (chunk / 8) * (RP * 128) + row * 128 + (chunk % 8) * 16) =
         make_uint4(0, 0, 0, 0);
   }
@@ -221,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_expect_tx(&sh.q_full, R * D * 2);
       for (int c = 0; c < D / 64; ++c)
         tma_load_3d(q_s + c * RP * 128, &tq, &sh.q_full, c * 64, kvh * g, bi * a.sq);
-      int issued = 0;
+      int k_issued = 0, v_issued = 0;
       for (int j = 0; j < n; ++j) {
         const int pos = (t_first + j) * BK;
         const int pg = pos / a.page_size;
@@ -232,25 +250,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         const int row = page * a.page_size + pos % a.page_size;
-        const int st = j % ST;
-        const uint32_t ph = ((j / ST) & 1) ^ 1;
-        if (!wait_bar(sh, &sh.k_empty[st], ph, a.err)) break;
-        mbar_expect_tx(&sh.k_full[st], kTile);
+        const int ks = j % KST, vs = j % VST;
+        if (!wait_bar(sh, &sh.k_empty[ks], ((j / KST) & 1) ^ 1, a.err)) break;
+        mbar_expect_tx(&sh.k_full[ks], kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(k_s + st * kTile + c * BK * 128, &tk, &sh.k_full[st], c * 64, kvh, row);
-        if (!wait_bar(sh, &sh.v_empty[st], ph, a.err)) { issued = 2 * j + 1; break; }
-        mbar_expect_tx(&sh.v_full[st], kTile);
+          tma_load_3d(k_s + ks * kTile + c * BK * 128, &tk, &sh.k_full[ks], c * 64, kvh, row);
+        k_issued = j + 1;
+        if (!wait_bar(sh, &sh.v_empty[vs], ((j / VST) & 1) ^ 1, a.err)) break;
+        mbar_expect_tx(&sh.v_full[vs], kTile);
         for (int c = 0; c < D / 64; ++c)
-          tma_load_3d(v_s + st * kTile + c * BK * 128, &tv, &sh.v_full[st], c * 64, kvh, row);
-        issued = 2 * j + 2;
+          tma_load_3d(v_s + vs * kTile + c * BK * 128, &tv, &sh.v_full[vs], c * 64, kvh, row);
+        v_issued = j + 1;
       }
       if (*(volatile int *)&sh.abort) {
         int *noerr = nullptr;
         mbar_wait(&sh.q_full, 0, noerr);
-        for (int x = max(0, issued - 2 * ST); x < issued; ++x) {
-          const int j = x / 2, st = j % ST;
-          mbar_wait(x % 2 ? &sh.v_full[st] : &sh.k_full[st], (j / ST) & 1, noerr);
-        }
+        for (int j = max(0, k_issued - KST); j < k_issued; ++j)
+          mbar_wait(&sh.k_full[j % KST], (j / KST) & 1, noerr);
+        for (int j = max(0, v_issued - VST); j < v_issued; ++j)
+          mbar_wait(&sh.v_full[j % VST], (j / VST) & 1, noerr);
       }
     }
   } else if (warp == 1) {
@@ -262,8 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t q_addr = smem_u32(q_s), k_addr = smem_u32(k_s), v_addr = smem_u32(v_s);
       const uint32_t p_addr = smem_u32(p_s);
       auto issue_s = [&](int j) -> bool {
-        const int st = j % ST;
-        if (!wait_bar(sh, &sh.k_full[st], (j / ST) & 1, a.err)) return false;
+        const int st = j % KST;
+        if (!wait_bar(sh, &sh.k_full[st], (j / KST) & 1, a.err)) return false;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -283,16 +301,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < n; ++j) {
         if (j + 1 < n && !issue_s(j + 1)) break;
         if (!wait_bar(sh, &sh.p_full[j & 1], (j >> 1) & 1, a.err)) break;
-        const int st = j % ST;
-        if (!wait_bar(sh, &sh.v_full[st], (j / ST) & 1, a.err)) break;
+        const int st = j % VST;
+        if (!wait_bar(sh, &sh.v_full[st], (j / VST) & 1, a.err)) break;
         tc_fence_after();
         const uint32_t pb = p_addr + (j & 1) * C::kPBytes;
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-          // A = V^T (M = d, MN-major: 64-column blocks BK*128 bytes apart)
-          const uint64_t ad = smem_desc(v_addr + st * kTile + kk * 16 * 128, BK * 128, 1024);
-          const uint64_t bd = smem_desc(pb + (kk / 4) * (RP * 128) + (kk % 4) * 32, 16, 1024);
-          mma_ss(tmem + C::kColO, ad, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+        for (int h2 = 0; h2 < C::kOHalves; ++h2) {
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // A = V^T (M = 128 rows of d from column block 2 h2 on, MN-major:
+            // 64-column blocks BK*128 bytes apart)
+            const uint64_t ad = smem_desc(v_addr + st * kTile + h2 * 2 * (BK * 128) + kk * 16 * 128,
+                                          BK * 128, 1024);
+            const uint64_t bd = smem_desc(pb + (kk / 4) * (RP * 128) + (kk % 4) * 32, 16, 1024);
+            mma_ss(tmem + C::kColO + h2 * RP, ad, bd, id_o, (j > 0 || kk > 0) ? 1u : 0u);
+          }
         }
         mma_commit(&sh.o_done);
         mma_commit(&sh.v_empty[st]);
@@ -431,22 +454,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<uint16_t *>(pb + (off ^ (((off >> 7) & 7) << 4))) = pv[q];
       }
       if (j > 0 && any_rescale) {  // all threads agree: the maxima are shared
-        uint32_t ou[RP];
-        tmem_ld_rp<RP>(tmem + lane_off + C::kColO, ou);
-        tmem_wait_ld();
 #pragma unroll
-        for (int q = 0; q < RP; ++q) ou[q] = __float_as_uint(__uint_as_float(ou[q]) * alpha[q]);
-        tmem_st_rp<RP>(tmem + lane_off + C::kColO, ou);
+        for (int h2 = 0; h2 < C::kOHalves; ++h2) {
+          uint32_t ou[RP];
+          tmem_ld_rp<RP>(tmem + lane_off + C::kColO + h2 * RP, ou);
+          tmem_wait_ld();
+#pragma unroll
+          for (int q = 0; q < RP; ++q) ou[q] = __float_as_uint(__uint_as_float(ou[q]) * alpha[q]);
+          tmem_st_rp<RP>(tmem + lane_off + C::kColO + h2 * RP, ou);
+        }
         tmem_wait_st();
       }
       if (__any_sync(0xffffffffu, key >= L)) {
         // keys past the cache end: their V rows may hold anything, and 0 * NaN
         // would poison O^T, so zero them (the TMA load must have landed)
-        if (!wait_warp(sh, &sh.v_full[j % ST], (j / ST) & 1, a.err)) { ok = false; break; }
+        if (!wait_warp(sh, &sh.v_full[j % VST], (j / VST) & 1, a.err)) { ok = false; break; }
         if (key >= L) {
-          uint8_t *vr = v_s + (j % ST) * kTile + jl * 128;
+          uint8_t *vr = v_s + (j % VST) * kTile + jl * 128;
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
+          for (int c = 0; c < D / 64; ++c)
 #pragma unroll
             for (int u = 0; u < 8; ++u)
               *reinterpret_cast<uint4 *>(vr + c * BK * 128 + u * 16) = make_uint4(0, 0, 0, 0);
@@ -475,15 +501,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = wait_warp(sh, &sh.grp, n & 1, a.err);
     }
     if (ok) {
+#pragma unroll 1
+      for (int h2 = 0; h2 < C::kOHalves; ++h2) {
       uint32_t ou[RP];
-      if (n > 0) {
-        tmem_ld_rp<RP>(tmem + lane_off + C::kColO, ou);
+      if (n > 0) {  // warp-collective: every lane loads, only real columns store
+        tmem_ld_rp<RP>(tmem + lane_off + C::kColO + h2 * RP, ou);
         tmem_wait_ld();
       } else {
 #pragma unroll
         for (int q = 0; q < RP; ++q) ou[q] = 0u;
       }
-      const int dcol = jl;  // O^T row = head-dim column
+      const int dcol = jl + 128 * h2;  // O^T row = head-dim column
+      if (dcol >= D) continue;         // d = 64: rows 64-127 of O^T are not used
 #pragma unroll
       for (int q = 0; q < RP; ++q) {
         if (q >= R) continue;
@@ -493,14 +522,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float lse = lsum > 0.f ? (m_run[q] + __log2f(lsum)) * kLn2 : -INFINITY;
         if (a.num_splits == 1) {
           static_cast<T *>(a.o)[(((int64_t)bi * a.sq + r) * a.hq + h) * D + dcol] = Elem<T>::from_f(o);
-          if (jl == 0) a.lse[((int64_t)bi * a.hq + h) * a.sq + r] = lse;
+          if (dcol == 0) a.lse[((int64_t)bi * a.hq + h) * a.sq + r] = lse;
         } else {
           a.o_part[((((int64_t)split * a.b + bi) * a.sq + r) * a.hq + h) * D + dcol] = o;
-          if (jl == 0) a.lse_part[(((int64_t)split * a.b + bi) * a.hq + h) * a.sq + r] = lse;
+          if (dcol == 0) a.lse_part[(((int64_t)split * a.b + bi) * a.hq + h) * a.sq + r] = lse;
         }
       }
+      }
     } else {
-      store_empty_split<T>(a, split, bi, kvh, R, jl, 128);
+      store_empty_split<T, D>(a, split, bi, kvh, R, jl, 128);
     }
   }
   tc_fence_before();
@@ -508,9 +538,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-template <typename T, int RP>
+template <typename T, int D, int RP>
 cudaError_t decode_tc(const DecodeArgs &a, cudaStream_t st) {
-  using C = DecCfg<RP>;
+  using C = DecCfg<D, RP>;
   CUtensorMap tq, tk, tv;
   const int64_t pool_rows = (int64_t)a.num_pages * a.page_size;
   const int g = a.hq / a.hkv;
@@ -529,29 +559,40 @@ cudaError_t decode_tc(const DecodeArgs &a, cudaStream_t st) {
   if (!make_map_3d(&tk, a.k_cache, a.dtype, pool_rows, a.hkv, D, BK) ||
       !make_map_3d(&tv, a.v_cache, a.dtype, pool_rows, a.hkv, D, BK))
     return cudaErrorInvalidValue;
-  cudaError_t e = set_smem_once<decode_tc_kernel<T, RP>>(C::kSmem);
+  cudaError_t e = set_smem_once<decode_tc_kernel<T, D, RP>>(C::kSmem);
   if (e != cudaSuccess) return e;
   const int64_t grid = (int64_t)a.num_splits * a.hkv * a.b;
   if (grid > INT32_MAX) return cudaErrorInvalidValue;
-  debug_log("decode: decode_tc_kernel d=128, %d query rows (g*sq) padded to %d, %d-key tiles, "
-            "num_splits=%d (%d keys each), grid=%lld CTAs x %d threads", (a.hq / a.hkv) * a.sq,
-            RP, BK, a.num_splits, a.split_chunk, (long long)grid, kThreads);
-  decode_tc_kernel<T, RP><<<(unsigned)grid, kThreads, C::kSmem, st>>>(tq, tk, tv, a);
+  debug_log("decode: decode_tc_kernel d=%d, %d query rows (g*sq) padded to %d, %d-key tiles, "
+            "K/V rings of %d/%d stages, num_splits=%d (%d keys each), grid=%lld CTAs x %d threads",
+            D, (a.hq / a.hkv) * a.sq, RP, BK, C::KST, C::VST, a.num_splits, a.split_chunk,
+            (long long)grid, kThreads);
+  decode_tc_kernel<T, D, RP><<<(unsigned)grid, kThreads, C::kSmem, st>>>(tq, tk, tv, a);
   count_launches(1);
   return cudaGetLastError();
+}
+
+template <int D>
+cudaError_t decode_tc_d(const DecodeArgs &a, int R, cudaStream_t st) {
+  const bool bf = a.dtype == ATTN_BF16;
+  if (R <= 16) return bf ? decode_tc<__nv_bfloat16, D, 16>(a, st) : decode_tc<__half, D, 16>(a, st);
+  return bf ? decode_tc<__nv_bfloat16, D, 32>(a, st) : decode_tc<__half, D, 32>(a, st);
 }
 
 }  // namespace
 
 // Returns cudaErrorNotSupported when the shape is outside what this kernel
-// handles (d != 128, g * sq > 32, page_size % 128 != 0).
+// handles (d not 64, 128 or 256, g * sq > 32, page_size % 128 != 0).
 cudaError_t launch_decode_tc(const DecodeArgs &a, cudaStream_t st) {
   const int R = (a.hq / a.hkv) * a.sq;
-  if (a.d != D || R > 32 || a.page_size % BK != 0 || a.sq > 256 || a.hq / a.hkv > 256)
+  if (R > 32 || a.page_size % BK != 0 || a.sq > 256 || a.hq / a.hkv > 256)
     return cudaErrorNotSupported;
-  const bool bf = a.dtype == ATTN_BF16;
-  if (R <= 16) return bf ? decode_tc<__nv_bfloat16, 16>(a, st) : decode_tc<__half, 16>(a, st);
-  return bf ? decode_tc<__nv_bfloat16, 32>(a, st) : decode_tc<__half, 32>(a, st);
+  switch (a.d) {
+    case 64: return decode_tc_d<64>(a, R, st);
+    case 128: return decode_tc_d<128>(a, R, st);
+    case 256: return decode_tc_d<256>(a, R, st);
+  }
+  return cudaErrorNotSupported;
 }
 
 }  // namespace attn

@@ -58,6 +58,16 @@ def test_head_dims_and_dtypes(d, dtype):
     run_small(42, 3, 2, 2, 4, 4, d, 600, 256, dtype, 0, causal=True)
 
 
+@pytest.mark.parametrize("d", [64, 256])
+@pytest.mark.parametrize("num_splits", [1, 3])
+@pytest.mark.parametrize("sq,s_new", [(1, 1), (4, 4), (8, 0)])
+def test_head_dims_gqa_splits(d, num_splits, sq, s_new):
+    """d = 64 and 256 on the tensor-core decode: GQA 4:1, so g * sq = 4, 16
+    and 32 query rows per KV head (both padded widths), one and several
+    splits, ragged caches over 128-token pages."""
+    run_small(45, 3, sq, s_new, 8, 2, d, 700, 128, syn.BF16, num_splits, causal=True)
+
+
 @pytest.mark.parametrize("kw", [dict(causal=True, window=(100, 0)), dict(softcap=30.0),
                                 dict(causal=True, softcap=50.0)])
 def test_window_softcap(kw):
