@@ -619,27 +619,39 @@ __global__ void __launch_bounds__(kThreads, 1)
 // zero the dQ accumulator of the atomic mode.  One warp per (row, head).
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int64_t rows) {
-  constexpr int V = D / 32;  // values per lane
+  // four (row, head) pairs per warp, eight lanes each: D/8 values a lane in
+  // 16-byte loads, so each warp keeps several loads of both streams in flight
+  constexpr int V = D / 8;  // values per lane
   const FwdArgs &f = a.f;
+  const int lane = threadIdx.x & 31, sub = lane & 7;
   const int64_t w = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-  for (int64_t x = w; x < rows * f.hq; x += nw) {
-    const int64_t row = x / f.hq;
-    const int h = (int)(x % f.hq);
-    const int64_t off = x * D + lane * V;
-    float o[V], g[V];
-    load_vec<T, V>(static_cast<const T *>(f.o) + off, o);
-    load_vec<T, V>(static_cast<const T *>(a.dout) + off, g);
+  const int64_t n = rows * f.hq;
+  for (int64_t x0 = w * 4; x0 < n; x0 += nw * 4) {
+    const int64_t x = x0 + (lane >> 3);
+    const bool live = x < n;
+    const int64_t off = (live ? x : 0) * D + sub * V;
     float s = 0.f;
 #pragma unroll
-    for (int e = 0; e < V; ++e) s = fmaf(o[e], g[e], s);
-    s = warp_sum(s);
-    if (!a.deterministic) {
+    for (int c = 0; c < V; c += 8) {
+      float o[8], g[8];
+      load_vec<T, 8>(static_cast<const T *>(f.o) + off + c, o);
+      load_vec<T, 8>(static_cast<const T *>(a.dout) + off + c, g);
 #pragma unroll
-      for (int e = 0; e < V; ++e) a.dq_acc[off + e] = 0.f;
+      for (int e = 0; e < 8; ++e) s = fmaf(o[e], g[e], s);
     }
-    if (lane == 0) {
+    s += __shfl_xor_sync(0xffffffffu, s, 4);
+    s += __shfl_xor_sync(0xffffffffu, s, 2);
+    s += __shfl_xor_sync(0xffffffffu, s, 1);
+    if (!live) continue;
+    if (!a.deterministic) {
+      float4 *z = reinterpret_cast<float4 *>(a.dq_acc + off);
+#pragma unroll
+      for (int c = 0; c < V / 4; ++c) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (sub == 0) {
+      const int64_t row = x / f.hq;
+      const int h = (int)(x % f.hq);
       int64_t li;
       if (f.seqs.cu_q) {
         li = (int64_t)h * f.seqs.total_q + row;
@@ -654,21 +666,24 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(BwdArgs a, int64_t rows) 
 }
 
 // dQ = scale * dQ_acc -> dtype: the accumulator is (hq, rows, d), dQ
-// (rows, hq, d) with rows dq_rs elements apart.  One thread per 4 values.
+// (rows, hq, d) with rows dq_rs elements apart.  One thread per 8 values
+// (two 16-byte loads, one 16-byte store).
 template <typename T, int D>
-__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdArgs a, int64_t rows, int64_t n4) {
+__global__ void __launch_bounds__(256) bwd_dq_convert_kernel(BwdArgs a, int64_t rows, int64_t n8) {
   const int hq = a.f.hq;
-  for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n4;
+  for (int64_t x = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; x < n8;
        x += (int64_t)gridDim.x * blockDim.x) {
-    // x walks dQ in (row, head, d / 4) order
-    const int c4 = (int)(x % (D / 4));
-    const int64_t rh = x / (D / 4);
+    // x walks dQ in (row, head, d / 8) order
+    const int c8 = (int)(x % (D / 8));
+    const int64_t rh = x / (D / 8);
     const int h = (int)(rh % hq);
     const int64_t row = rh / hq;
-    const float4 v = reinterpret_cast<const float4 *>(a.dq_acc)[(h * rows + row) * (D / 4) + c4];
+    const float4 *src = reinterpret_cast<const float4 *>(a.dq_acc) + ((h * rows + row) * (D / 8) + c8) * 2;
+    const float4 v0 = src[0], v1 = src[1];
     const float s = a.f.scale;
-    uint2 out{Elem<T>::from_f2(v.x * s, v.y * s), Elem<T>::from_f2(v.z * s, v.w * s)};
-    *reinterpret_cast<uint2 *>(static_cast<T *>(a.dq) + row * a.dq_rs + (int64_t)h * D + c4 * 4) =
+    const uint4 out{Elem<T>::from_f2(v0.x * s, v0.y * s), Elem<T>::from_f2(v0.z * s, v0.w * s),
+                    Elem<T>::from_f2(v1.x * s, v1.y * s), Elem<T>::from_f2(v1.z * s, v1.w * s)};
+    *reinterpret_cast<uint4 *>(static_cast<T *>(a.dq) + row * a.dq_rs + (int64_t)h * D + c8 * 8) =
         out;
   }
 }
@@ -680,7 +695,7 @@ cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
   const FwdArgs &f = a.f;
   const int64_t rows_q = f.seqs.cu_q ? f.seqs.total_q : (int64_t)f.batch * f.seqs.sq;
   const int64_t rows_k = f.seqs.cu_k ? f.seqs.total_k : (int64_t)f.batch * f.seqs.sk;
-  const int prep_blocks = (int)std::min<int64_t>((rows_q * f.hq + 7) / 8, (int64_t)sms * 16);
+  const int prep_blocks = (int)std::min<int64_t>((rows_q * f.hq + 31) / 32, (int64_t)sms * 16);
   if (rows_q > 0) {
     bwd_prep_kernel<T, D><<<std::max(prep_blocks, 1), 256, 0, st>>>(a, rows_q);
     count_launches(1);
@@ -717,9 +732,9 @@ cudaError_t bwd_tc(const BwdArgs &a, int sms, cudaStream_t st) {
     cudaError_t e = launch_bwd_dq_tc(a, st);
     if (e != cudaSuccess) return e;
   } else if (rows_q > 0) {
-    const int64_t n4 = rows_q * f.hq * D / 4;
-    const int blocks = (int)std::min<int64_t>((n4 + 255) / 256, (int64_t)sms * 16);
-    bwd_dq_convert_kernel<T, D><<<std::max(blocks, 1), 256, 0, st>>>(a, rows_q, n4);
+    const int64_t n8 = rows_q * f.hq * D / 8;
+    const int blocks = (int)std::min<int64_t>((n8 + 255) / 256, (int64_t)sms * 16);
+    bwd_dq_convert_kernel<T, D><<<std::max(blocks, 1), 256, 0, st>>>(a, rows_q, n8);
     count_launches(1);
   }
   return cudaGetLastError();

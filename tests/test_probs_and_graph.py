@@ -138,3 +138,54 @@ def test_decode_step_captured_in_cuda_graph():
         seqlens = seqlens + s_new
     assert_close(host(out), ro, dtype, "graph step out")
     assert_lse(host(lse), rl)
+
+
+@pytest.mark.parametrize("d,window", [(128, (-1, -1)), (128, (200, 0)), (64, (-1, -1))])
+def test_training_step_captured_in_cuda_graph(d, window):
+    """FAQ Q19: a forward + deterministic backward step captured once in a
+    CUDA graph and replayed on new inputs (same buffers) gives the eager
+    call's bits: the library allocates nothing and never synchronises, and
+    its per-device set-up runs on the first, eager, call.  Both forward
+    layouts at d = 128 (two 128-row tiles; one tile with two CTAs per SM
+    under the window) and the d = 64 one."""
+    import torch
+
+    from exact_attention_41_gb300 import libattn
+
+    b, s, hq, hkv = 2, 1536, 8, 2
+    kw = dict(causal=True, window=window)
+    bufs = {n: dev(syn.dense_case(60 + i, b, s, s, hq, hkv, d, syn.BF16, with_dout=True)[n],
+                   syn.BF16) for i, n in enumerate(("q", "k", "v", "dout"))}
+    q, k, v, do = (bufs[n] for n in ("q", "k", "v", "dout"))
+    o = torch.empty_like(q)
+    lse = torch.empty((b, hq, s), device="cuda", dtype=torch.float32)
+    ws = libattn.bwd_workspace(q, k, True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+    def step():
+        libattn.fwd(q, k, v, out=o, lse=lse, **kw)
+        libattn.bwd(q, k, v, o, lse, do, deterministic=True, workspace=ws, dq=dq, dk=dk, dv=dv,
+                    **kw)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    torch.cuda.synchronize()
+    for t in range(2):
+        case = syn.dense_case(70 + t, b, s, s, hq, hkv, d, syn.BF16, with_dout=True)
+        for n in ("q", "k", "v", "dout"):
+            bufs[n].copy_(dev(case[n], syn.BF16))
+        g.replay()
+        torch.cuda.synchronize()
+        got = [x.clone() for x in (o, lse, dq, dk, dv)]
+        step()
+        torch.cuda.synchronize()
+        for x, y in zip(got, (o, lse, dq, dk, dv)):
+            assert torch.equal(x, y)
