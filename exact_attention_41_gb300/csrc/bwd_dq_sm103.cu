@@ -53,7 +53,7 @@ struct DqCfg {
   static constexpr uint32_t kColS = 0, kColDP = 2 * BN, kColDQ = 3 * BN;
   static constexpr int kQTile = BM * D * 2;        // Q or dO of the tile: 32 KB at d = 128
   static constexpr int kKTile = BN * D * 2;        // one K or V tile
-  static constexpr int kSmemData = 2 * kQTile + (KST + VST) * kKTile;  // 224 KB
+  static constexpr int kSmemData = 2 * kQTile + (KST + VST) * kKTile;  // 224 KB at d = 128, 256
   static constexpr int kSmem = kSmemData + 1024;
   static_assert(kSmem <= 227 * 1024 - 1024, "shared memory");
   static_assert(kColDQ + DO <= 512, "TMEM");

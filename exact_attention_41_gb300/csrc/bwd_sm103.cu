@@ -75,7 +75,7 @@ struct BwdCfg {
   static constexpr int kDsRow = BQ * 2;          // bytes per key row of a dS^T array
   static constexpr int kDS = BN * kDsRow;        // one 16-bit [key][query] array
   static constexpr uint32_t kDsSwizzle = BQ == 64 ? 2 : 4;  // descriptor: 128- / 64-byte swizzle
-  static constexpr int kSmemData = 2 * kTileK + ST * 2 * kChunk + 2 * 2 * kDS;  // 224 KB
+  static constexpr int kSmemData = 2 * kTileK + ST * 2 * kChunk + 2 * 2 * kDS;  // 224 KB at d = 128, 256
   static constexpr int kSmem = kSmemData + 1024;
   static_assert(kSmem <= 227 * 1024 - 1024, "shared memory");
 };

@@ -15,7 +15,8 @@
 // page (page_size % 128 == 0), fetched by TMA from the page pool at the
 // physical row the block table gives.  Roles:
 //
-//   warp 0     TMA producer (Q once, then K and V tiles, 3-stage ring)
+//   warp 0     TMA producer (Q once, then K and V tiles through 3-stage
+//              rings; 2 and 1 stages at d = 256)
 //   warp 1     MMA issuer
 //   warps 2-5  one thread per key (TMEM lane): mask, column max across the
 //              CTA, exp, P into shared memory; the same threads own the d
