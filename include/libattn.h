@@ -193,7 +193,9 @@ attn_status attn_bwd_varlen(const void *q, const void *k, const void *v, const v
  * keys with the bottom-right mask (query r sits at position L_i - sq + r).
  * Every L_i must fit max_pages_per_seq * page_size; the block_table entries
  * used must lie in [0, num_pages) (checked on the device: the device error
- * word is raised and the entry's output is left unwritten).
+ * word is raised, and a split that meets a bad entry contributes the empty
+ * result -- O = 0, LSE = -inf -- so the output is deterministic but not
+ * meaningful for that batch entry).
  *
  * q (b,sq,hq,d), out (b,sq,hq,d), lse (b,hq,sq) fp32.
  *
