@@ -693,7 +693,8 @@ def run_profile_case(args):
     fwd / bwd   causal bf16 b=1 s=8192 hq=32 hkv=8 d=128 (`--deterministic`
                 for that backward mode; `--head-dim` 64 or 256 keeps
                 hq * d = 4096 and hkv = hq / 4, as the head-dim sweep does)
-    decode      paged decode b=16, sq=s_new=4 (--decode-sq), hq=32 hkv=8, caches U[1,32768]
+    decode      paged decode b=16, sq=s_new=4 (--decode-sq), hq=32 hkv=8, d=128
+                (--head-dim 64 / 256 keep hq and hkv), caches U[1,32768]
                 in 256-token pages (the workload's per-entry shape; 16 entries
                 make several full waves of splits)
     varlen      the varlen workload (64 sequences U[100,4096], window (256,0),
@@ -738,13 +739,13 @@ def run_profile_case(args):
             libattn.bwd_varlen(q, k, v, o, lse, do, cu, cu, mx, mx,
                                deterministic=args.deterministic, **kw)
     else:
-        b, sq, page = 16, args.decode_sq, 256
+        b, sq, page, d = 16, args.decode_sq, 256, args.head_dim
         seqlens, table, npages = syn.decode_layout(9, b, 32768, page, sq)
-        kc = syn.device_normal((npages, page, HKV, D), bf, 5)
-        vc = syn.device_normal((npages, page, HKV, D), bf, 6)
-        q = syn.device_normal((b, sq, HQ, D), bf, 7)
-        kn = syn.device_normal((b, sq, HKV, D), bf, 8)
-        vn = syn.device_normal((b, sq, HKV, D), bf, 9)
+        kc = syn.device_normal((npages, page, HKV, d), bf, 5)
+        vc = syn.device_normal((npages, page, HKV, d), bf, 6)
+        q = syn.device_normal((b, sq, HQ, d), bf, 7)
+        kn = syn.device_normal((b, sq, HKV, d), bf, 8)
+        vn = syn.device_normal((b, sq, HKV, d), bf, 9)
         sl = torch.from_numpy(seqlens).cuda()
         bt = torch.from_numpy(table).cuda()
         for _ in range(args.calls):
@@ -770,7 +771,7 @@ def main():
     ap.add_argument("--deterministic", action="store_true", help="--profile-case bwd mode")
     ap.add_argument("--decode-sq", type=int, default=4, help="--profile-case decode: sq = s_new")
     ap.add_argument("--head-dim", type=int, default=128, choices=[64, 128, 256],
-                    help="--profile-case fwd/bwd: head dim (hq = 4096 / d)")
+                    help="--profile-case fwd/bwd: head dim (hq = 4096 / d); decode: head dim")
     args = ap.parse_args()
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
