@@ -45,12 +45,16 @@ def _dense_call(kind, case, dtype, deterministic=False):
 
 
 @pytest.mark.parametrize("kind,deterministic", [("fwd", False), ("bwd", False), ("bwd", True)])
-def test_wait_timeout_is_reported_and_recoverable(kind, deterministic):
+@pytest.mark.parametrize("s,d", [(384, 128), (1280, 128), (384, 64), (384, 256)])
+def test_wait_timeout_is_reported_and_recoverable(kind, deterministic, s, d):
+    """Every tensor-core kernel layout: the one-tile two-CTA forward (s = 384)
+    and the two-tile one (1280 keys) at d = 128, the d = 64 and d = 256
+    forwards, and the backward kernels at each head dim."""
     import torch
 
     from exact_attention_41_gb300 import libattn
 
-    case = syn.dense_case(51, 2, 384, 384, 8, 2, 128, syn.BF16, with_dout=True)
+    case = syn.dense_case(51, 2, s, s, 8, 2, d, syn.BF16, with_dout=True)
     _clear()
     prev = libattn.set_wait_limit_ns(1_000_000)
     libattn.set_test_stall(True)
@@ -68,22 +72,23 @@ def test_wait_timeout_is_reported_and_recoverable(kind, deterministic):
     assert libattn.device_error() == (0, 0)
     q, k, v = (f64(case[x], syn.BF16) for x in ("q", "k", "v"))
     if kind == "fwd":
-        ro, rl = ref.forward(q, k, v, 1 / math.sqrt(128), causal=True)
+        ro, rl = ref.forward(q, k, v, 1 / math.sqrt(d), causal=True)
         assert_close(host(out[0]), ro, syn.BF16, "out")
         assert_lse(host(out[1]), rl)
     else:
-        rq, rk, rv = ref.backward(q, k, v, f64(case["dout"], syn.BF16), 1 / math.sqrt(128),
+        rq, rk, rv = ref.backward(q, k, v, f64(case["dout"], syn.BF16), 1 / math.sqrt(d),
                                   causal=True, stored_o=syn.BF16)
         for g, r, n in zip(out, (rq, rk, rv), ("dq", "dk", "dv")):
             assert_close(host(g), r, syn.BF16, n)
 
 
-def test_decode_wait_timeout_is_reported_and_recoverable():
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_decode_wait_timeout_is_reported_and_recoverable(d):
     import torch
 
     from exact_attention_41_gb300 import libattn
 
-    c = syn.decode_case(52, 3, 1, 1, 8, 2, 128, 900, 128, syn.BF16)
+    c = syn.decode_case(52, 3, 1, 1, 8, 2, d, 900, 128, syn.BF16)
     kc, vc = dev(c["k_cache"], syn.BF16), dev(c["v_cache"], syn.BF16)
     args = (dev(c["q"], syn.BF16), kc, vc, dev_i32(c["cache_seqlens"]))
     kw = dict(k_new=dev(c["k_new"], syn.BF16), v_new=dev(c["v_new"], syn.BF16),
@@ -104,7 +109,7 @@ def test_decode_wait_timeout_is_reported_and_recoverable():
     assert libattn.device_error() == (0, 0)
     ro, rl, _, _ = ref.kvcache_forward(
         f64(c["q"], syn.BF16), f64(c["k_cache"], syn.BF16), f64(c["v_cache"], syn.BF16),
-        c["cache_seqlens"], 1 / math.sqrt(128), f64(c["k_new"], syn.BF16),
+        c["cache_seqlens"], 1 / math.sqrt(d), f64(c["k_new"], syn.BF16),
         f64(c["v_new"], syn.BF16), c["block_table"], 128, causal=True)
     assert_close(host(o), ro, syn.BF16, "out")
     assert_lse(host(lse), rl)
