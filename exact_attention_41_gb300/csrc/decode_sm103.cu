@@ -16,7 +16,7 @@
 // physical row the block table gives.  Roles:
 //
 //   warp 0     TMA producer (Q once, then K and V tiles through 3-stage
-//              rings; 2 and 1 stages at d = 256)
+//              rings; other depths at d = 64 and 256, below)
 //   warp 1     MMA issuer
 //   warps 2-5  one thread per key (TMEM lane): mask, column max across the
 //              CTA, exp, P into shared memory; the same threads own the d
@@ -27,9 +27,9 @@
 //
 // Head dims: at d = 64 the O^T product keeps M = 128 (its rows 64-127 read
 // the 16 KB after the V tile, padding included in the shared memory, and are
-// never stored); at d = 256 O^T is two M = 128 products, one per half of d,
-// and the 64 KB K and V tiles come through a 2-stage K ring and a 1-stage V
-// ring.
+// never stored; with 16 query rows two CTAs share an SM, each with 2-stage
+// rings); at d = 256 O^T is two M = 128 products, one per half of d, and the
+// 64 KB K and V tiles come through a 1-stage K ring and a 2-stage V ring.
 #include <cudaTypedefs.h>
 
 #include "kernels.h"
@@ -47,8 +47,11 @@ constexpr float kRescaleThreshold = 8.0f;
 // Shapes for head dim D and RP (query rows padded to 16 or 32).
 template <int D, int RP>
 struct DecCfg {
-  static constexpr int KST = D == 256 ? 2 : 3;       // K ring stages
-  static constexpr int VST = D == 256 ? 1 : 3;       // V ring stages
+  // two CTAs per SM at d = 64 with 16 query rows (its registers allow it):
+  // the per-tile chain of one overlaps the other's
+  static constexpr int kCtas = (D == 64 && RP == 16) ? 2 : 1;
+  static constexpr int KST = D == 256 ? 1 : kCtas == 2 ? 2 : 3;  // K ring stages
+  static constexpr int VST = D == 256 ? 2 : kCtas == 2 ? 2 : 3;  // V ring stages
   static constexpr int kTile = BK * D * 2;           // one K or V tile: 32 KB at d = 128
   static constexpr int kQBytes = RP * D * 2;
   static constexpr int kPBytes = RP * BK * 2;
@@ -60,6 +63,7 @@ struct DecCfg {
   static constexpr uint32_t kColO = 2 * RP;          // O^T: kOHalves blocks of RP columns
   static constexpr uint32_t kTmemCols = (2 + kOHalves) * RP <= 64 ? 64 : 128;
   static_assert(kSmem + 2048 <= 227 * 1024, "shared memory");
+  static_assert(kCtas == 1 || 2 * (kSmem + 2048) <= 228 * 1024, "shared memory of two CTAs");
 };
 
 template <int KST, int VST>
@@ -155,7 +159,7 @@ __device__ __forceinline__ void tmem_st_rp(uint32_t taddr, uint32_t (&r)[RP]) {
 }
 
 template <typename T, int D, int RP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, DecCfg<D, RP>::kCtas)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                      const __grid_constant__ CUtensorMap tv, const DecodeArgs a) {
   using C = DecCfg<D, RP>;
